@@ -1,0 +1,429 @@
+"""Benchmark of the GB300 W4A16 MoE layer: MoE-layer tokens/s, INT4 weight-stream
+GB/s and roofline fraction, one JSON line on stdout (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode1]
+                    [--impl ours|reference]
+
+A step is one forward of the whole layer (router, histogram/scan/permute,
+gate/up+SwiGLU, down, combine with the shared expert) over one batch. The
+default workload is decode at 1 token on the DeepSeek-V4-Flash-shaped layer
+(hidden 4096, 256 routed experts top-6 + 1 shared, intermediate 2048, INT4
+g128). Inputs are synthetic (seeded), resident in HBM before timing; the L2
+is flushed (a 512 MB write) before every timed step, outside the timed span.
+The forward is captured once in a CUDA graph and replayed.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import moe_synth as ms  # noqa: E402
+
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------ algorithmic work
+def expert_bytes(shape, inter):
+    H = shape.hidden
+    w13 = 2 * inter * H // 2 + 2 * inter * (H // 128) * 2
+    w2 = H * inter // 2 + H * (inter // 128) * 2
+    return w13, w2
+
+
+def layer_work(shape, counts):
+    """Algorithmic bytes and flops of one forward given per-expert row counts."""
+    T, H, E, k, I, Is = (shape.tokens, shape.hidden, shape.experts, shape.top_k, shape.inter,
+                         shape.shared_inter)
+    hit = int((np.asarray(counts) > 0).sum())
+    r13, r2 = expert_bytes(shape, I)
+    s13, s2 = expert_bytes(shape, Is) if Is else (0, 0)
+    w13_bytes = hit * r13 + s13
+    w2_bytes = hit * r2 + s2
+    act = T * H * 2 * 2                      # x in, out
+    router = E * H * 4 + E * 4
+    flops = 2 * T * E * H + 2 * 3 * H * (T * k * I + (T * Is if Is else 0))
+    return {"hit": hit, "w13_bytes": w13_bytes, "w2_bytes": w2_bytes,
+            "weight_bytes": w13_bytes + w2_bytes, "act_bytes": act, "router_bytes": router,
+            "bytes": w13_bytes + w2_bytes + act + router, "flops": flops}
+
+
+def kernel_bytes(name, shape, work):
+    """Algorithmic DRAM bytes of one launch of a kernel (weights it must stream)."""
+    T, H, E, k, I = shape.tokens, shape.hidden, shape.experts, shape.top_k, shape.inter
+    rows = T * k + T
+    if name.startswith("gemv_gate_up") or name.startswith("tc_gate_up"):
+        return work["w13_bytes"] + T * H * 2 + rows * max(I, shape.shared_inter) * 2
+    if name.startswith("gemv_down") or name.startswith("tc_down"):
+        return work["w2_bytes"] + rows * max(I, shape.shared_inter) * 2 + rows * H * 4
+    if name.startswith("route") or name.startswith("router"):
+        return work["router_bytes"] + T * H * 2 * 2
+    if name == "combine":
+        return rows * H * 4 + T * H * 2
+    return 0
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        self.path = f"/tmp/moe_bench_clocks_{os.getpid()}.csv"
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={q}", "--format=csv,noheader",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1].split()[0]))
+                smax = float(f[2].split()[0])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- ncu traffic
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source is unchanged since the capture (else None)."""
+    path = os.path.join(PROFILE_DIR, f"{kernel}_{workload}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        prof = json.load(f)
+    src = os.path.join(ROOT, "w4a16_routed_expert_router_gb300", "csrc", prof.get("source", ""))
+    if not os.path.exists(src):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if digest != prof.get("source_sha256_16"):
+        return None
+    return prof.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def maybe_init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def max_over_ranks(value, dist, device=None):
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle arm
+def oracle_sample(shape, budget_s=15.0):
+    """Time the fp64 oracle on the host on a bounded sample of the workload.
+
+    Routing is computed for the whole batch; outputs token by token until the
+    time budget is spent. Drawing the synthetic weights is not timed.
+    """
+    from oracle import moe_oracle as mo
+    x = ms.tokens(shape)
+    rw, rb = ms.router_weights(shape), ms.router_bias(shape)
+    shared = ms.expert_weights(shape, shape.experts) if shape.shared_inter else None
+    wall = cpu = 0.0
+    t0, c0 = time.perf_counter(), time.process_time()
+    route = mo.route(x, rw, rb, shape.experts, shape.top_k)
+    wall += time.perf_counter() - t0
+    cpu += time.process_time() - c0
+    done = 0
+    while wall < budget_s and (done < shape.tokens or shape.tokens < 8):
+        if done and done % shape.tokens == 0:   # tiny batches: time further draws
+            x = ms.tokens(dataclasses.replace(shape, token_seed=shape.token_seed + 7919 * done))
+            t0, c0 = time.perf_counter(), time.process_time()
+            route = mo.route(x, rw, rb, shape.experts, shape.top_k)
+            wall += time.perf_counter() - t0
+            cpu += time.process_time() - c0
+        t = done % shape.tokens
+        experts = [None] * shape.experts
+        for e in route["ids"][t]:
+            experts[int(e)] = ms.expert_weights(shape, int(e))
+        t0, c0 = time.perf_counter(), time.process_time()
+        mo.moe_forward(x[t:t + 1], rw, rb, experts, shared, shape.top_k)
+        wall += time.perf_counter() - t0
+        cpu += time.process_time() - c0
+        done += 1
+    return {"tokens": done, "wall_s": wall, "cpu_s": cpu,
+            "cores": max(1, round(cpu / wall)) if wall > 0 else 1}
+
+
+def run_reference(args, shape):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    r = oracle_sample(shape, budget_s=max(5.0, min(60.0, 10.0 + 2.0 * args.steps)))
+    value = r["tokens"] / r["wall_s"]
+    sample = (f"{r['tokens']} tokens of {shape.name} batches (routing of every batch, "
+              f"outputs token by token), {r['wall_s']:.1f} s wall")
+    line = {"impl": "reference", "metric": "moe_layer_tokens_per_s", "value": value,
+            "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * r["wall_s"] / max(r["tokens"], 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": shape.name, "tokens": shape.tokens, "hidden": shape.hidden,
+                       "experts": shape.experts, "top_k": shape.top_k, "inter": shape.inter,
+                       "shared_inter": shape.shared_inter},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": r["cores"],
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- GPU arm
+def run_ours(args, shape):
+    import torch
+
+    import w4a16_routed_expert_router_gb300 as moe
+    from moe_synth.device import upload_layer, upload_tokens
+    from w4a16_routed_expert_router_gb300 import _build
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = maybe_init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    moe.lib()
+
+    layer = ms.make_layer(shape)          # weights + tokens (unguarded draw)
+    tensors = upload_layer(layer, dev)[0]
+    T, H = shape.tokens, shape.hidden
+    steps = args.steps
+    # distinct token batches (same distribution), resident in HBM before timing
+    nx = min(steps, 8)
+    xs = [upload_tokens(ms.tokens(dataclasses.replace(shape, token_seed=shape.token_seed + 7919 * i)),
+                        dev) for i in range(nx)]
+    out = torch.empty((T, H), dtype=torch.int16, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    obj = moe.MoeLayer(shape.hidden, shape.experts, shape.top_k, shape.inter,
+                       shape.shared_inter, T, tensors)
+    prof = moe.MoeLayer(shape.hidden, shape.experts, shape.top_k, shape.inter,
+                        shape.shared_inter, T, tensors, flags=moe.MOE_W4A16_FLAG_PROFILE)
+    stream = torch.cuda.Stream(device=dev)
+    xin = torch.empty_like(xs[0])
+
+    # --- capture one forward in a CUDA graph (input copied into xin first)
+    with torch.cuda.stream(stream):
+        xin.copy_(xs[0])
+        obj.forward(xin, out, stream=stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        obj.forward(xin, out, stream=torch.cuda.current_stream())
+    launches_per_fwd = len(moe.moe_w4a16_last_launches(obj.handle))
+
+    def step(i, timed, ev=None):
+        with torch.cuda.stream(stream):
+            flush.fill_(float(i))
+            xin.copy_(xs[i % nx])
+            if timed:
+                ev[0].record(stream)
+            graph.replay()
+            if timed:
+                ev[1].record(stream)
+
+    for i in range(args.warmup):
+        step(i, False)
+    stream.synchronize()
+    assert moe.moe_w4a16_check_device_errors(obj.handle) == 0
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(steps):
+            step(i, True, evs[i])
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    per_step = [a.elapsed_time(b) for a, b in evs]
+    total_ms = sum(per_step)
+    total_ms = max_over_ranks(total_ms, dist, dev)
+    ms_per_step = total_ms / steps
+    value = world * T * steps / (total_ms / 1000.0)
+
+    # --- routing stats of the timed inputs (for the algorithmic bytes)
+    rt_counts = []
+    for i in range(nx):
+        with torch.cuda.stream(stream):
+            obj.forward(xs[i], out, stream=stream)
+        stream.synchronize()
+        rt_counts.append(np.diff(obj.routing(T, stream=stream)["offsets"]))
+    works = [layer_work(shape, c) for c in rt_counts]
+    work = {k_: float(np.mean([w[k_] for w in works])) for k_ in works[0]}
+
+    # --- per-kernel durations with CUDA events (no graph), same flush
+    kernel_ms = {}
+    nprof = min(steps, 50)
+    for i in range(args.warmup + nprof):
+        with torch.cuda.stream(stream):
+            flush.fill_(float(i))
+            prof.forward(xs[i % nx], out, stream=stream)
+        stream.synchronize()
+        if i >= args.warmup:
+            for name, t_ms in moe.moe_w4a16_last_launches(prof.handle):
+                kernel_ms.setdefault(name, []).append(t_ms)
+    kernel_avg = {n: float(np.mean(v)) for n, v in kernel_ms.items()}
+    dominant = max(kernel_avg, key=kernel_avg.get)
+
+    # --- end to end through the host-buffer entry point
+    xh = torch.from_numpy(ms.tokens(shape).view(np.int16)).pin_memory()
+    oh = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    for _ in range(3):
+        obj.forward_host(xh, oh, stream=stream)
+    e2e_s = 0.0
+    n_e2e = min(steps, 100)
+    for i in range(n_e2e):
+        with torch.cuda.stream(stream):
+            flush.fill_(float(i))
+        stream.synchronize()
+        t0 = time.perf_counter()
+        obj.forward_host(xh, oh, stream=stream)
+        e2e_s += time.perf_counter() - t0
+    e2e_s = max_over_ranks(e2e_s, dist, dev)
+    e2e_value = world * T * n_e2e / e2e_s
+
+    pk = peaks()
+    dom_bytes = kernel_bytes(dominant, shape, work)
+    dom_s = kernel_avg[dominant] / 1000.0
+    achieved = dom_bytes / dom_s / 1e9
+    traffic = profiled_traffic(dominant, shape.name)
+    layer_roof_s = max(work["bytes"] / (pk["hbm_gbs"] * 1e9),
+                       work["flops"] / (pk["bf16_tflops"] * 1e12))
+    clk = clocks.summary()
+
+    if rank == 0:
+        cpu = oracle_sample(shape, budget_s=15.0) if world == 1 else None
+        line = {
+            "metric": "moe_layer_tokens_per_s", "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": shape.name, "tokens": T, "hidden": H,
+                       "experts": shape.experts, "top_k": shape.top_k, "inter": shape.inter,
+                       "shared_inter": shape.shared_inter, "weights": "int4 g128 symmetric",
+                       "l2": "flushed before every step (512 MB write, untimed)",
+                       "graph": "one forward per CUDA-graph replay", "parallelism": "replicas"},
+            "weight_stream_gbs": work["weight_bytes"] / (ms_per_step / 1000.0) / 1e9,
+            "layer_roofline_frac": layer_roof_s / (ms_per_step / 1000.0),
+            "experts_hit": work["hit"],
+            "roofline": {"kernel": dominant, "bound": "hbm", "achieved": achieved,
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                         "traffic": traffic, "algorithmic_bytes": dom_bytes,
+                         "peak_source": pk["source"]},
+            "kernels_ms": kernel_avg,
+            "gpu_launches": launches_per_fwd * steps,
+            "clocks": clk,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
+                    "d2h_bytes_per_step": T * H * 2},
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = {"value": cpu["tokens"] / cpu["wall_s"], "unit": "tokens/s",
+                                    "cores": cpu["cores"], "kind": "oracle",
+                                    "sample": f"{cpu['tokens']} tokens of {shape.name} batches "
+                                              f"({cpu['wall_s']:.1f} s wall)"}
+        print(json.dumps(line), flush=True)
+    obj.close()
+    prof.close()
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="decode1", choices=ms.CONFIG_ORDER)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    shape = ms.CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, shape)
+    else:
+        run_ours(args, shape)
+
+
+if __name__ == "__main__":
+    main()

@@ -187,7 +187,7 @@ def moe_forward(x_bits, router_w, router_b, experts, shared, k: int,
     E = len(experts)
     r = route(x_bits, router_w, router_b, E, k)
     T = r["ids"].shape[0]
-    subset = np.arange(T) if token_subset is None else np.asarray(token_subset)
+    subset = np.arange(T) if token_subset is None else np.asarray(token_subset, dtype=np.int64)
     x = bf16_to_f64(x_bits)[subset]
     out = np.zeros_like(x)
     if shared is not None and subset.size:

@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+declared symbol, and invalid arguments are rejected before any device work.
+No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import w4a16_routed_expert_router_gb300 as moe
+from w4a16_routed_expert_router_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "moe_w4a16.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return moe.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(moe_w4a16_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert _declared() == sorted(moe.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    assert moe.moe_w4a16_status_string(0) == "ok"
+    assert "max_tokens" in moe.moe_w4a16_status_string(moe.MOE_W4A16_ERR_TOO_MANY_TOKENS)
+    assert moe.moe_w4a16_status_string(-99) == "unknown status"
+
+
+def _cfg(**kw):
+    base = dict(hidden=4096, num_experts=256, top_k=6, inter=2048, shared_inter=2048,
+                max_tokens=64, flags=0)
+    base.update(kw)
+    return moe.make_config(**base)
+
+
+def test_workspace_bytes_of_a_valid_config(L):
+    n = moe.moe_w4a16_workspace_bytes(_cfg())
+    # at least: logits, activations copy, h, y for 64 tokens
+    T, k, H, I, E = 64, 6, 4096, 2048, 256
+    rows = T * k + T
+    assert n >= T * E * 4 + T * H * 2 + rows * I * 2 + rows * H * 4
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(hidden=4000), moe.MOE_W4A16_ERR_UNSUPPORTED_SHAPE),
+    (dict(hidden=0), moe.MOE_W4A16_ERR_UNSUPPORTED_SHAPE),
+    (dict(inter=100), moe.MOE_W4A16_ERR_UNSUPPORTED_SHAPE),
+    (dict(shared_inter=-128), moe.MOE_W4A16_ERR_UNSUPPORTED_SHAPE),
+    (dict(num_experts=0), moe.MOE_W4A16_ERR_UNSUPPORTED_SHAPE),
+    (dict(num_experts=257), moe.MOE_W4A16_ERR_UNSUPPORTED_SHAPE),
+    (dict(top_k=0), moe.MOE_W4A16_ERR_UNSUPPORTED_SHAPE),
+    (dict(top_k=9), moe.MOE_W4A16_ERR_UNSUPPORTED_SHAPE),
+    (dict(num_experts=4, top_k=5), moe.MOE_W4A16_ERR_UNSUPPORTED_SHAPE),
+    (dict(max_tokens=0), moe.MOE_W4A16_ERR_INVALID_ARG),
+    (dict(flags=0x100), moe.MOE_W4A16_ERR_INVALID_ARG),
+    (dict(flags=moe.MOE_W4A16_FLAG_FORCE_GEMV | moe.MOE_W4A16_FLAG_FORCE_TC),
+     moe.MOE_W4A16_ERR_INVALID_ARG),
+])
+def test_invalid_configs_are_rejected(L, kw, status):
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_w4a16_workspace_bytes(_cfg(**kw))
+    assert ei.value.status == status
+    h = ctypes.c_void_p()
+    assert L.moe_w4a16_create(ctypes.byref(_cfg(**kw)), 0, ctypes.byref(h)) == status
+    assert not h.value
+
+
+def test_group_size_must_be_128(L):
+    c = _cfg()
+    c.group_size = 64
+    n = ctypes.c_size_t()
+    assert L.moe_w4a16_workspace_bytes(ctypes.byref(c), ctypes.byref(n)) == \
+        moe.MOE_W4A16_ERR_UNSUPPORTED_SHAPE
+
+
+def test_null_handle_and_out_pointers(L):
+    assert L.moe_w4a16_create(ctypes.byref(_cfg()), 0, None) == moe.MOE_W4A16_ERR_INVALID_ARG
+    w = moe.moe_w4a16_weights()
+    assert L.moe_w4a16_forward(None, None, 1, ctypes.byref(w), None, None) == \
+        moe.MOE_W4A16_ERR_INVALID_ARG
+    assert L.moe_w4a16_destroy(None) == moe.MOE_W4A16_OK
+    assert L.moe_w4a16_get_routing(None, None, None, None, None, None, None) == \
+        moe.MOE_W4A16_ERR_INVALID_ARG
+
+
+def test_create_without_a_gpu_reports_no_device(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    assert L.moe_w4a16_create(ctypes.byref(_cfg()), 0, ctypes.byref(h)) == \
+        moe.MOE_W4A16_ERR_NO_DEVICE

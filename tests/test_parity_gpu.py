@@ -1,0 +1,176 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small cases compare every output; the full-size V4-Flash-shaped workloads
+compare routing for every token and outputs on sampled tokens.
+"""
+import numpy as np
+import pytest
+
+import moe_synth as ms
+from moe_synth.device import upload_layer, upload_tokens
+from tests import moe_cases as mc
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu, pytest.mark.timeout(1800)]
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import w4a16_routed_expert_router_gb300 as moe  # noqa: E402
+from w4a16_routed_expert_router_gb300 import _build  # noqa: E402
+
+_build.build()
+DEV = "cuda:0"
+
+
+def _layer_obj(layer, tensors, max_tokens, flags=0, bias=None):
+    s = layer.shape
+    t = dict(tensors)
+    if bias is not None:
+        t["router_bias"] = torch.from_numpy(np.asarray(bias, np.float32)).to(DEV)
+    return moe.MoeLayer(s.hidden, s.experts, s.top_k, s.inter, s.shared_inter, max_tokens, t,
+                        flags=flags)
+
+
+def _run(obj, x_bits):
+    x = upload_tokens(x_bits, DEV)
+    out = obj.forward(x)
+    torch.cuda.synchronize()
+    assert moe.moe_w4a16_check_device_errors(obj.handle) == 0
+    return out.cpu().numpy(), obj.routing(x_bits.shape[0])
+
+
+# ------------------------------------------------------------------ tiny layer
+@pytest.fixture(scope="module")
+def tiny():
+    shape = ms.CONFIGS["tiny16"]
+    base = mc.weights_of(shape)
+    tensors = upload_layer(base, DEV)[0]
+    return shape, tensors
+
+
+@pytest.mark.parametrize("T", [16, 1, 2, 3, 7, 8, 9, 15, 17, 31, 33, 63, 64, 65, 100, 129, 200])
+def test_tiny_layer_parity(tiny, T):
+    shape, tensors = tiny
+    layer = mc.layer_with_tokens(shape, T)
+    ref = mc.oracle(layer)
+    obj = _layer_obj(layer, tensors, max_tokens=256)
+    out, rt = _run(obj, layer.x)
+    mc.check_routing(rt, ref, shape.experts)
+    mc.check_output(out, ref["out"])
+    obj.close()
+
+
+def test_tiny_one_expert_takes_every_token(tiny):
+    shape, tensors = tiny
+    bias = np.zeros(shape.experts, np.float32)
+    bias[3] = 4.0
+    layer = mc.layer_with_tokens(shape, 40, bias=bias)
+    ref = mc.oracle(layer)
+    assert (ref["ids"][:, 0] == 3).all()
+    obj = _layer_obj(layer, tensors, 64, bias=bias)
+    out, rt = _run(obj, layer.x)
+    assert rt["offsets"][4] - rt["offsets"][3] == 40
+    mc.check_routing(rt, ref, shape.experts)
+    mc.check_output(out, ref["out"])
+    obj.close()
+
+
+def test_tiny_empty_batch_and_limits(tiny):
+    shape, tensors = tiny
+    layer = mc.layer_with_tokens(shape, 4)
+    obj = _layer_obj(layer, tensors, 8)
+    x = torch.zeros((0, shape.hidden), dtype=torch.int16, device=DEV)
+    out = obj.forward(x)
+    assert out.shape == (0, shape.hidden)
+    assert moe.moe_w4a16_last_launches(obj.handle) == []
+    big = torch.zeros((9, shape.hidden), dtype=torch.int16, device=DEV)
+    with pytest.raises(moe.MoeError) as ei:
+        obj.forward(big)
+    assert ei.value.status == moe.MOE_W4A16_ERR_TOO_MANY_TOKENS
+    # misaligned activation pointer
+    raw = torch.zeros((4 * shape.hidden + 8,), dtype=torch.int16, device=DEV)
+    out = torch.empty((4, shape.hidden), dtype=torch.int16, device=DEV)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_w4a16_forward(obj.handle, raw.data_ptr() + 2, 4, obj.weights, out.data_ptr(), 0)
+    assert ei.value.status == moe.MOE_W4A16_ERR_MISALIGNED
+    # aliasing input and output
+    xx = upload_tokens(layer.x, DEV)
+    with pytest.raises(moe.MoeError):
+        moe.moe_w4a16_forward(obj.handle, xx.data_ptr(), 4, obj.weights, xx.data_ptr(), 0)
+    assert moe.moe_w4a16_check_device_errors(obj.handle) == 0
+    obj.close()
+
+
+def test_tiny_deterministic_and_batch_invariant(tiny):
+    shape, tensors = tiny
+    layer = mc.layer_with_tokens(shape, 48)
+    obj = _layer_obj(layer, tensors, 64)
+    a, _ = _run(obj, layer.x)
+    b, _ = _run(obj, layer.x)
+    np.testing.assert_array_equal(a, b)
+    c, _ = _run(obj, layer.x[:5])
+    np.testing.assert_array_equal(c, a[:5])
+    obj.close()
+
+
+def test_tiny_forward_host_matches_device(tiny):
+    shape, tensors = tiny
+    layer = mc.layer_with_tokens(shape, 16)
+    obj = _layer_obj(layer, tensors, 16)
+    a, _ = _run(obj, layer.x)
+    xh = torch.from_numpy(layer.x.view(np.int16)).pin_memory()
+    oh = torch.empty((16, shape.hidden), dtype=torch.int16).pin_memory()
+    obj.forward_host(xh, oh)
+    np.testing.assert_array_equal(oh.numpy(), a)
+    obj.close()
+
+
+# ------------------------------------------------------------ full-size layer
+@pytest.fixture(scope="module")
+def full():
+    shape = ms.CONFIGS["decode1"]
+    base = mc.weights_of(shape)
+    tensors = upload_layer(base, DEV)[0]
+    return tensors
+
+
+def _full_case(full, name, sample):
+    shape = ms.CONFIGS[name]
+    layer = mc.layer_with_tokens(shape)
+    route = mc.oracle(layer, subset=[])
+    T = shape.tokens
+    subset = sample(route, T)
+    ref = mc.oracle(layer, subset=subset)
+    obj = _layer_obj(layer, full, T, bias=layer.router_b)
+    out, rt = _run(obj, layer.x)
+    mc.check_routing(rt, route, shape.experts)
+    mc.check_output(out[subset], ref["out"])
+    names = [n for n, _ in moe.moe_w4a16_last_launches(obj.handle)]
+    obj.close()
+    return rt, names
+
+
+def test_decode1_full_layer(full):
+    rt, names = _full_case(full, "decode1", lambda r, T: np.arange(T))
+    assert names == ["route_small", "gemv_gate_up_swiglu", "gemv_down", "combine"]
+
+
+def test_decode64_routing_and_sampled_outputs(full):
+    _full_case(full, "decode64", lambda r, T: np.array([0, 1, 17, 31, 32, 45, 62, 63]))
+
+
+def test_zipf2048_routing_and_sampled_outputs(full):
+    def sample(r, T):
+        hot = int(np.argmax(r["counts"]))
+        first_hot = int(np.nonzero((r["ids"] == hot).any(axis=1))[0][0])
+        cold = int(np.argmin(np.where(r["counts"] > 0, r["counts"], 1 << 30)))
+        first_cold = int(np.nonzero((r["ids"] == cold).any(axis=1))[0][0])
+        return np.unique([0, first_hot, first_cold, 1023, T - 1])
+    rt, _ = _full_case(full, "zipf2048", sample)
+    counts = np.diff(rt["offsets"])
+    assert counts.max() >= 1800 and (counts < 10).sum() >= 60
+
+
+def test_prefill8192_routing_and_sampled_outputs(full):
+    _full_case(full, "prefill8192", lambda r, T: np.array([0, 4095, 8191]))

@@ -1,0 +1,58 @@
+// Internal interface between the C-ABI layer and the kernel translation units.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kSmallT = 64;       // <= this many tokens: single-kernel router
+constexpr int kTopkTokens = 64;   // tokens per CTA in the large-T router
+constexpr int kPassRows = 16;     // expert rows per GEMV task (two 8-token MMA blocks)
+constexpr int kTile1 = 16;        // gate (and up) channels per gate/up GEMV task
+constexpr int kTile2 = 32;        // output channels per down GEMV task
+constexpr int kGemvStages = 8;    // TMA pipeline depth of the GEMV kernels
+constexpr int kGemvThreads = 288; // 8 consumer warps + 1 TMA producer warp
+
+// Records the kernels one forward launches (and their CUDA events when
+// profiling is on).
+struct LaunchLog {
+  static constexpr int kMax = 16;
+  int n = 0;
+  const char* names[kMax];
+  cudaEvent_t* events = nullptr;  // 2 * kMax events, or null
+  void begin(const char* name, cudaStream_t s) {
+    if (n < kMax) {
+      names[n] = name;
+      if (events) cudaEventRecord(events[2 * n], s);
+    }
+  }
+  void end(cudaStream_t s) {
+    if (n < kMax) {
+      if (events) cudaEventRecord(events[2 * n + 1], s);
+      ++n;
+    }
+  }
+};
+
+// Expert weights of one GEMV pass (gate/up or down).
+struct GemvWeights {
+  const uint16_t* scale_routed;
+  const uint16_t* scale_shared;
+  CUtensorMap tm_routed;
+  CUtensorMap tm_shared;
+};
+
+cudaError_t launch_route(const Dims& d, const Routing& r, const uint16_t* x, const float* router_w,
+                         const float* bias, uint16_t* xg, cudaStream_t s, LaunchLog& log);
+
+cudaError_t gemv_setup(int* ctas_per_sm);
+cudaError_t launch_gemv_gate_up(const Dims& d, const Routing& r, const GemvWeights& w,
+                                const uint16_t* xg, uint16_t* h, int hstride, int grid,
+                                cudaStream_t s, LaunchLog& log);
+cudaError_t launch_gemv_down(const Dims& d, const Routing& r, const GemvWeights& w,
+                             const uint16_t* h, int hstride, float* y, int grid, cudaStream_t s,
+                             LaunchLog& log);
+cudaError_t launch_combine(const Dims& d, const Routing& r, const float* y, uint16_t* out,
+                           cudaStream_t s, LaunchLog& log);
+
+}  // namespace moe

@@ -1,0 +1,418 @@
+// C ABI of the W4A16 MoE layer: argument validation, workspace, tensor maps,
+// dispatch of the router / expert / combine kernels.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/moe_w4a16.h"
+#include "kernels.h"
+
+using namespace moe;
+
+struct moe_w4a16_handle {
+  moe_w4a16_config cfg;
+  int device = 0;
+  int num_sms = 0;
+  int gemv_grid = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  Routing r{};
+  uint16_t* xg = nullptr;
+  uint16_t* h = nullptr;
+  int hstride = 0;
+  float* y = nullptr;
+  uint16_t* x_dev = nullptr;    // forward_host staging
+  uint16_t* out_dev = nullptr;
+  int last_T = 0;
+  LaunchLog log;
+  cudaEvent_t events[2 * LaunchLog::kMax];
+  bool events_made = false;
+  // tensor-map cache keyed by the weight pointers it was encoded for
+  const void* map_keys[4] = {nullptr, nullptr, nullptr, nullptr};
+  CUtensorMap maps[4];
+};
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+int validate_config(const moe_w4a16_config* c) {
+  if (!c) return MOE_W4A16_ERR_INVALID_ARG;
+  if (c->flags & ~(MOE_W4A16_FLAG_FORCE_GEMV | MOE_W4A16_FLAG_FORCE_TC | MOE_W4A16_FLAG_PROFILE))
+    return MOE_W4A16_ERR_INVALID_ARG;
+  if ((c->flags & MOE_W4A16_FLAG_FORCE_GEMV) && (c->flags & MOE_W4A16_FLAG_FORCE_TC))
+    return MOE_W4A16_ERR_INVALID_ARG;
+  if (c->max_tokens < 1 || c->max_tokens > (1 << 20)) return MOE_W4A16_ERR_INVALID_ARG;
+  if (c->group_size != kGroup) return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
+  if (c->hidden < 128 || c->hidden > 16384 || c->hidden % 128) return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
+  if (c->inter < 128 || c->inter > 16384 || c->inter % 128) return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
+  if (c->shared_inter < 0 || c->shared_inter > 16384 || c->shared_inter % 128)
+    return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
+  if (c->num_experts < 1 || c->num_experts > kMaxExperts) return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
+  if (c->top_k < 1 || c->top_k > kMaxTopK || c->top_k > c->num_experts)
+    return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
+  // row counts of the stacked expert tensors must fit the int32 row indices
+  if ((long long)c->num_experts * 2 * c->inter >= (1LL << 31) ||
+      (long long)c->num_experts * c->hidden >= (1LL << 31))
+    return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
+  return MOE_W4A16_OK;
+}
+
+struct Layout {
+  size_t off[32];
+  size_t total;
+};
+
+// Workspace carve-up; the order is the order of the fields filled in create().
+Layout plan(const moe_w4a16_config& c) {
+  const size_t Tm = c.max_tokens, E = c.num_experts, k = c.top_k, H = c.hidden;
+  const size_t rows = Tm * k + Tm;
+  const size_t hstride = c.inter > c.shared_inter ? c.inter : c.shared_inter;
+  const size_t nblk = (Tm + kTopkTokens - 1) / kTopkTokens;
+  const size_t sizes[] = {
+      Tm * E * 4,            // 0 logits
+      Tm * k * 4,            // 1 ids
+      Tm * k * 4,            // 2 wts
+      E * 4,                 // 3 counts
+      (E + 1) * 4,           // 4 offsets
+      (E + 1) * 4,           // 5 active
+      kMetaWords * 4,        // 6 meta
+      (E + 2) * 4,           // 7 task1
+      (E + 2) * 4,           // 8 task2
+      Tm * k * 4,            // 9 perm
+      Tm * k * 4,            // 10 inv
+      nblk * E * 4,          // 11 blockcnt
+      nblk * E * 4,          // 12 blockbase
+      kTickets * 4,          // 13 tickets
+      4,                     // 14 err
+      Tm * H * 2,            // 15 xg
+      rows * hstride * 2,    // 16 h
+      rows * H * 4,          // 17 y
+      Tm * H * 2,            // 18 x_dev
+      Tm * H * 2,            // 19 out_dev
+  };
+  Layout L;
+  size_t o = 0;
+  for (size_t i = 0; i < sizeof(sizes) / sizeof(sizes[0]); ++i) {
+    L.off[i] = o;
+    o += align256(sizes[i]);
+  }
+  L.total = o;
+  return L;
+}
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_W4A16_OK;
+  fprintf(stderr, "moe_w4a16: CUDA error %s\n", cudaGetErrorString(e));
+  return MOE_W4A16_ERR_CUDA;
+}
+
+// 3-D view {16 words of one K-group, K-groups, rows} of a packed INT4 tensor
+// [rows, K/8] uint32, box {16, 1, 16}: one 128-wide K-group of 16 rows.
+int encode_int4_map(CUtensorMap* m, const void* base, long long rows, int K) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MOE_W4A16_ERR_CUDA;
+  cuuint64_t dims[3] = {16, (cuuint64_t)(K / kGroup), (cuuint64_t)rows};
+  cuuint64_t strides[2] = {64, (cuuint64_t)K / 2};  // bytes: group, row
+  cuuint32_t box[3] = {16, 1, 16};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    fprintf(stderr, "moe_w4a16: cuTensorMapEncodeTiled failed (%d)\n", (int)r);
+    return MOE_W4A16_ERR_CUDA;
+  }
+  return MOE_W4A16_OK;
+}
+
+int get_map(moe_w4a16_handle* h, int slot, const void* base, long long rows, int K) {
+  if (h->map_keys[slot] == base && base) return MOE_W4A16_OK;
+  const int st = encode_int4_map(&h->maps[slot], base, rows, K);
+  if (st == MOE_W4A16_OK) h->map_keys[slot] = base;
+  return st;
+}
+
+int validate_weights(const moe_w4a16_config& c, const moe_w4a16_weights* w) {
+  if (!w) return MOE_W4A16_ERR_INVALID_ARG;
+  const void* req[] = {w->router_w, w->router_bias, w->w13_q, w->w13_s, w->w2_q, w->w2_s};
+  for (const void* p : req) {
+    if (!p) return MOE_W4A16_ERR_INVALID_ARG;
+    if (!aligned16(p)) return MOE_W4A16_ERR_MISALIGNED;
+  }
+  if (c.shared_inter > 0) {
+    const void* sh[] = {w->sh_w13_q, w->sh_w13_s, w->sh_w2_q, w->sh_w2_s};
+    for (const void* p : sh) {
+      if (!p) return MOE_W4A16_ERR_INVALID_ARG;
+      if (!aligned16(p)) return MOE_W4A16_ERR_MISALIGNED;
+    }
+  }
+  return MOE_W4A16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_w4a16_status_string(int s) {
+  switch (s) {
+    case MOE_W4A16_OK: return "ok";
+    case MOE_W4A16_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_W4A16_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_W4A16_ERR_TOO_MANY_TOKENS: return "num_tokens exceeds max_tokens";
+    case MOE_W4A16_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case MOE_W4A16_ERR_CUDA: return "CUDA error";
+    case MOE_W4A16_ERR_DEVICE: return "device error flag set";
+    case MOE_W4A16_ERR_NO_DEVICE: return "no usable sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+int moe_w4a16_workspace_bytes(const moe_w4a16_config* cfg, size_t* bytes) {
+  const int st = validate_config(cfg);
+  if (st != MOE_W4A16_OK) return st;
+  if (!bytes) return MOE_W4A16_ERR_INVALID_ARG;
+  *bytes = plan(*cfg).total;
+  return MOE_W4A16_OK;
+}
+
+int moe_w4a16_create(const moe_w4a16_config* cfg, int device, moe_w4a16_handle** out) {
+  if (!out) return MOE_W4A16_ERR_INVALID_ARG;
+  *out = nullptr;
+  int st = validate_config(cfg);
+  if (st != MOE_W4A16_OK) return st;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev <= 0) {
+    cudaGetLastError();
+    return MOE_W4A16_ERR_NO_DEVICE;
+  }
+  if (device < 0 || device >= ndev) return MOE_W4A16_ERR_INVALID_ARG;
+  cudaDeviceProp prop;
+  if ((st = cuda_status(cudaGetDeviceProperties(&prop, device))) != MOE_W4A16_OK) return st;
+  if (prop.major != 10 || prop.minor != 3) return MOE_W4A16_ERR_NO_DEVICE;
+  if ((st = cuda_status(cudaSetDevice(device))) != MOE_W4A16_OK) return st;
+
+  moe_w4a16_handle* h = new (std::nothrow) moe_w4a16_handle();
+  if (!h) return MOE_W4A16_ERR_CUDA;
+  h->cfg = *cfg;
+  h->device = device;
+  h->num_sms = prop.multiProcessorCount;
+  int per_sm = 0;
+  if ((st = cuda_status(gemv_setup(&per_sm))) != MOE_W4A16_OK || per_sm < 1) {
+    delete h;
+    return st != MOE_W4A16_OK ? st : MOE_W4A16_ERR_CUDA;
+  }
+  h->gemv_grid = h->num_sms * per_sm;
+
+  const Layout L = plan(*cfg);
+  if ((st = cuda_status(cudaMalloc(&h->ws, L.total))) != MOE_W4A16_OK) {
+    delete h;
+    return st;
+  }
+  h->ws_bytes = L.total;
+  cudaMemset(h->ws, 0, L.total);
+  uint8_t* b = static_cast<uint8_t*>(h->ws);
+  Routing& r = h->r;
+  r.logits = reinterpret_cast<float*>(b + L.off[0]);
+  r.ids = reinterpret_cast<int*>(b + L.off[1]);
+  r.wts = reinterpret_cast<float*>(b + L.off[2]);
+  r.counts = reinterpret_cast<int*>(b + L.off[3]);
+  r.offsets = reinterpret_cast<int*>(b + L.off[4]);
+  r.active = reinterpret_cast<int*>(b + L.off[5]);
+  r.meta = reinterpret_cast<int*>(b + L.off[6]);
+  r.task1 = reinterpret_cast<int*>(b + L.off[7]);
+  r.task2 = reinterpret_cast<int*>(b + L.off[8]);
+  r.perm = reinterpret_cast<int*>(b + L.off[9]);
+  r.inv = reinterpret_cast<int*>(b + L.off[10]);
+  r.blockcnt = reinterpret_cast<int*>(b + L.off[11]);
+  r.blockbase = reinterpret_cast<int*>(b + L.off[12]);
+  r.tickets = reinterpret_cast<unsigned*>(b + L.off[13]);
+  r.err = reinterpret_cast<unsigned*>(b + L.off[14]);
+  h->xg = reinterpret_cast<uint16_t*>(b + L.off[15]);
+  h->h = reinterpret_cast<uint16_t*>(b + L.off[16]);
+  h->hstride = cfg->inter > cfg->shared_inter ? cfg->inter : cfg->shared_inter;
+  h->y = reinterpret_cast<float*>(b + L.off[17]);
+  h->x_dev = reinterpret_cast<uint16_t*>(b + L.off[18]);
+  h->out_dev = reinterpret_cast<uint16_t*>(b + L.off[19]);
+
+  if (cfg->flags & MOE_W4A16_FLAG_PROFILE) {
+    for (int i = 0; i < 2 * LaunchLog::kMax; ++i) cudaEventCreate(&h->events[i]);
+    h->events_made = true;
+  }
+  if ((st = cuda_status(cudaDeviceSynchronize())) != MOE_W4A16_OK) {
+    moe_w4a16_destroy(h);
+    return st;
+  }
+  *out = h;
+  return MOE_W4A16_OK;
+}
+
+int moe_w4a16_destroy(moe_w4a16_handle* h) {
+  if (!h) return MOE_W4A16_OK;
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  if (h->events_made)
+    for (int i = 0; i < 2 * LaunchLog::kMax; ++i) cudaEventDestroy(h->events[i]);
+  if (h->ws) cudaFree(h->ws);
+  delete h;
+  return MOE_W4A16_OK;
+}
+
+int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t T, const moe_w4a16_weights* w,
+                      uint16_t* out, void* stream) {
+  if (!h) return MOE_W4A16_ERR_INVALID_ARG;
+  const moe_w4a16_config& c = h->cfg;
+  if (T < 0) return MOE_W4A16_ERR_INVALID_ARG;
+  if (T > c.max_tokens) return MOE_W4A16_ERR_TOO_MANY_TOKENS;
+  int st = validate_weights(c, w);
+  if (st != MOE_W4A16_OK) return st;
+  h->log.n = 0;
+  h->log.events = h->events_made ? h->events : nullptr;
+  if (T == 0) {
+    h->last_T = 0;
+    return MOE_W4A16_OK;
+  }
+  if (!x || !out) return MOE_W4A16_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out)) return MOE_W4A16_ERR_MISALIGNED;
+  {
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), oa = reinterpret_cast<uintptr_t>(out);
+    const uintptr_t n = (uintptr_t)T * c.hidden * 2;
+    if (xa < oa + n && oa < xa + n) return MOE_W4A16_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) cudaSetDevice(h->device);
+
+  Dims d{T, c.hidden, c.num_experts, c.top_k, c.inter, c.shared_inter};
+  // tensor maps (cached per weight pointer)
+  GemvWeights g1, g2;
+  if ((st = get_map(h, 0, w->w13_q, (long long)c.num_experts * 2 * c.inter, c.hidden)) != MOE_W4A16_OK)
+    return st;
+  if ((st = get_map(h, 1, w->w2_q, (long long)c.num_experts * c.hidden, c.inter)) != MOE_W4A16_OK)
+    return st;
+  if (c.shared_inter > 0) {
+    if ((st = get_map(h, 2, w->sh_w13_q, 2LL * c.shared_inter, c.hidden)) != MOE_W4A16_OK) return st;
+    if ((st = get_map(h, 3, w->sh_w2_q, c.hidden, c.shared_inter)) != MOE_W4A16_OK) return st;
+  }
+  g1.tm_routed = h->maps[0];
+  g1.tm_shared = c.shared_inter > 0 ? h->maps[2] : h->maps[0];
+  g1.scale_routed = w->w13_s;
+  g1.scale_shared = c.shared_inter > 0 ? w->sh_w13_s : w->w13_s;
+  g2.tm_routed = h->maps[1];
+  g2.tm_shared = c.shared_inter > 0 ? h->maps[3] : h->maps[1];
+  g2.scale_routed = w->w2_s;
+  g2.scale_shared = c.shared_inter > 0 ? w->sh_w2_s : w->w2_s;
+
+  cudaError_t e;
+  if ((e = launch_route(d, h->r, x, w->router_w, w->router_bias, h->xg, s, h->log)) != cudaSuccess)
+    return cuda_status(e);
+  if ((e = launch_gemv_gate_up(d, h->r, g1, h->xg, h->h, h->hstride, h->gemv_grid, s, h->log)) !=
+      cudaSuccess)
+    return cuda_status(e);
+  if ((e = launch_gemv_down(d, h->r, g2, h->h, h->hstride, h->y, h->gemv_grid, s, h->log)) !=
+      cudaSuccess)
+    return cuda_status(e);
+  if ((e = launch_combine(d, h->r, h->y, out, s, h->log)) != cudaSuccess) return cuda_status(e);
+  h->last_T = T;
+  return MOE_W4A16_OK;
+}
+
+int moe_w4a16_forward_host(moe_w4a16_handle* h, const uint16_t* x_host, int32_t T,
+                           const moe_w4a16_weights* w, uint16_t* out_host, void* stream) {
+  if (!h) return MOE_W4A16_ERR_INVALID_ARG;
+  if (T < 0) return MOE_W4A16_ERR_INVALID_ARG;
+  if (T > h->cfg.max_tokens) return MOE_W4A16_ERR_TOO_MANY_TOKENS;
+  if (T > 0 && (!x_host || !out_host)) return MOE_W4A16_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t n = (size_t)T * h->cfg.hidden * 2;
+  int st;
+  if (T > 0) {
+    cudaSetDevice(h->device);
+    if ((st = cuda_status(cudaMemcpyAsync(h->x_dev, x_host, n, cudaMemcpyHostToDevice, s))) !=
+        MOE_W4A16_OK)
+      return st;
+  }
+  if ((st = moe_w4a16_forward(h, h->x_dev, T, w, h->out_dev, stream)) != MOE_W4A16_OK) return st;
+  if (T > 0) {
+    if ((st = cuda_status(cudaMemcpyAsync(out_host, h->out_dev, n, cudaMemcpyDeviceToHost, s))) !=
+        MOE_W4A16_OK)
+      return st;
+  }
+  return cuda_status(cudaStreamSynchronize(s));
+}
+
+int moe_w4a16_get_routing(moe_w4a16_handle* h, int32_t* ids, float* wts, int32_t* offsets,
+                          int32_t* perm, int32_t* inv, void* stream) {
+  if (!h) return MOE_W4A16_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t tk = (size_t)h->last_T * h->cfg.top_k * 4;
+  cudaError_t e = cudaSuccess;
+  if (ids && tk && e == cudaSuccess) e = cudaMemcpyAsync(ids, h->r.ids, tk, cudaMemcpyDeviceToDevice, s);
+  if (wts && tk && e == cudaSuccess) e = cudaMemcpyAsync(wts, h->r.wts, tk, cudaMemcpyDeviceToDevice, s);
+  if (perm && tk && e == cudaSuccess)
+    e = cudaMemcpyAsync(perm, h->r.perm, tk, cudaMemcpyDeviceToDevice, s);
+  if (inv && tk && e == cudaSuccess) e = cudaMemcpyAsync(inv, h->r.inv, tk, cudaMemcpyDeviceToDevice, s);
+  if (offsets && e == cudaSuccess) {
+    if (h->last_T > 0)
+      e = cudaMemcpyAsync(offsets, h->r.offsets, (h->cfg.num_experts + 1) * 4,
+                          cudaMemcpyDeviceToDevice, s);
+    else
+      e = cudaMemsetAsync(offsets, 0, (h->cfg.num_experts + 1) * 4, s);
+  }
+  return cuda_status(e);
+}
+
+int moe_w4a16_check_device_errors(moe_w4a16_handle* h, uint32_t* flags) {
+  if (!h) return MOE_W4A16_ERR_INVALID_ARG;
+  cudaSetDevice(h->device);
+  int st;
+  if ((st = cuda_status(cudaDeviceSynchronize())) != MOE_W4A16_OK) return st;
+  uint32_t v = 0;
+  if ((st = cuda_status(cudaMemcpy(&v, h->r.err, 4, cudaMemcpyDeviceToHost))) != MOE_W4A16_OK)
+    return st;
+  if (v && (st = cuda_status(cudaMemset(h->r.err, 0, 4))) != MOE_W4A16_OK) return st;
+  if (flags) *flags = v;
+  return v ? MOE_W4A16_ERR_DEVICE : MOE_W4A16_OK;
+}
+
+int moe_w4a16_last_launches(moe_w4a16_handle* h, int32_t* count, const char** names, float* ms,
+                            int32_t capacity) {
+  if (!h || capacity < 0) return MOE_W4A16_ERR_INVALID_ARG;
+  const int n = h->log.n;
+  if (count) *count = n;
+  for (int i = 0; i < n && i < capacity; ++i) {
+    if (names) names[i] = h->log.names[i];
+    if (ms) {
+      ms[i] = -1.f;
+      if (h->events_made) {
+        float v = 0.f;
+        if (cudaEventElapsedTime(&v, h->events[2 * i], h->events[2 * i + 1]) == cudaSuccess) ms[i] = v;
+        else cudaGetLastError();
+      }
+    }
+  }
+  return MOE_W4A16_OK;
+}
+
+}  // extern "C"

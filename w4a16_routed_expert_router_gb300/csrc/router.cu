@@ -1,0 +1,488 @@
+// Router of the W4A16 MoE layer: fp32 logits, sigmoid + bias top-k selection,
+// renormalised combine weights, per-expert histogram, exclusive scan and the
+// stable token permutation that gives every expert a contiguous row segment.
+//
+// "canada-quant/DeepSeek-V4-Flash-W4A16-FP8-MTP", table "Component
+// precisions": the router bias ffn.gate.bias is fp32, so the router runs in
+// fp32 end to end. "What does everyone get wrong about optimizing DeepSeek V4
+// Flash ...", section "Sparse architecture": six of 256 routed experts are
+// active per token.
+//
+// Two paths:
+//  * small T (<= kSmallT tokens): one kernel. Every CTA streams a slice of the
+//    fp32 router weight (the only large read at decode sizes); the CTA that
+//    finishes last (atomic ticket, no waiting) does top-k, histogram, scan,
+//    placement and the expert task lists for all tokens.
+//  * large T: a tiled fp32 logits kernel, a top-k kernel (warp per token, CTA
+//    histograms, last CTA scans), and a placement kernel that ranks each
+//    CTA's items stably with warp match/ballot.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+// Expert kernels' task decomposition: gate/up tasks cover 16 channels of
+// gate and 16 of up; down tasks cover 32 output channels; one task handles up
+// to kPassRows rows of an expert's segment.
+__device__ __forceinline__ int passes_for(int rows) { return (rows + kPassRows - 1) / kPassRows; }
+
+// Warp-wide top-k of one token. Lane l holds experts l, l+32, ...; returns in
+// lanes 0..k-1 the chosen expert (descending sel, ties -> lower index) and its
+// unbiased score.
+__device__ __forceinline__ void warp_topk(const float* logit_row, const float* bias, int E, int k,
+                                          int lane, int* out_id, float* out_w) {
+  constexpr int kPer = kMaxExperts / 32;
+  float sel[kPer], sc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float l = logit_row[e];
+      const float s = 1.0f / (1.0f + expf(-l));
+      sc[i] = s;
+      sel[i] = s + bias[e];
+    } else {
+      sc[i] = 0.f;
+      sel[i] = -INFINITY;
+    }
+  }
+  float chosen_s = 0.f;
+  int chosen_e = -1;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      if (sel[i] > bv || (sel[i] == bv && e < be)) {
+        bv = sel[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    // owner lane removes the winner and publishes its score
+    float ws = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (lane + 32 * i == be) {
+        ws = sc[i];
+        sel[i] = -INFINITY;
+      }
+    ws = __shfl_sync(0xffffffffu, ws, be & 31);
+    if (lane == j) {
+      chosen_e = be;
+      chosen_s = ws;
+    }
+  }
+  // renormalise over the chosen experts in slot order (bias not included)
+  float sum = 0.f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, chosen_s, j);
+  *out_id = chosen_e;
+  *out_w = chosen_s / sum;
+}
+
+// Exclusive scan of one value per thread across a 256-thread block.
+__device__ __forceinline__ int block_scan_256(int v, int* scratch /* >= 8 ints */, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) scratch[warp] = inc;
+  __syncthreads();
+  int base = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const int s = scratch[w];
+    if (w < warp) base += s;
+    tot += s;
+  }
+  __syncthreads();
+  *total = tot;
+  return base + inc - v;
+}
+
+// Active-expert list and task prefixes, run by one 256-thread block after the
+// counts are final. counts_s: shared [E]. Writes active/task1/task2/meta.
+__device__ void build_task_lists(const Dims& d, const int* counts_s, const Routing& r,
+                                 int* scratch) {
+  const int e = threadIdx.x;
+  const int c = (e < d.E) ? counts_s[e] : 0;
+  int n_act;
+  const int idx = block_scan_256(c > 0 ? 1 : 0, scratch, &n_act);
+  if (e < d.E && c > 0) r.active[idx] = e;
+  const int n_total = n_act + (d.Is > 0 ? 1 : 0);
+  if (threadIdx.x == 0 && d.Is > 0) r.active[n_act] = d.E;
+  __syncthreads();
+  // task prefix: a < n_total <= 257 entries, one per thread (+ one extra)
+  int tot1 = 0, tot2 = 0;
+  for (int base = 0; base < n_total; base += 256) {
+    const int a = base + threadIdx.x;
+    int c1 = 0, c2 = 0;
+    if (a < n_total) {
+      const int ex = r.active[a];
+      const bool sh = (ex == d.E);
+      const int rows = sh ? d.T : counts_s[ex];
+      const int p = passes_for(rows);
+      c1 = p * ((sh ? d.Is : d.I) / kTile1);
+      c2 = p * (d.H / kTile2);
+    }
+    int s1, s2;
+    const int x1 = block_scan_256(c1, scratch, &s1);
+    const int x2 = block_scan_256(c2, scratch, &s2);
+    if (a < n_total) {
+      r.task1[a] = tot1 + x1;
+      r.task2[a] = tot2 + x2;
+    }
+    tot1 += s1;
+    tot2 += s2;
+  }
+  if (threadIdx.x == 0) {
+    r.task1[n_total] = tot1;
+    r.task2[n_total] = tot2;
+    r.meta[kMetaActive] = n_total;
+    r.meta[kMetaTasks1] = tot1;
+    r.meta[kMetaTasks2] = tot2;
+  }
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------- small T
+// grid: ceil(E / 2) CTAs x 256 threads. Warps 0-3 score expert 2b, warps 4-7
+// expert 2b+1, each warp a quarter of H. Requires T <= kSmallT, H % 512 == 0.
+__global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __restrict__ x,
+                                                          const float* __restrict__ router_w,
+                                                          const float* __restrict__ bias,
+                                                          uint16_t* __restrict__ xg, Dims d,
+                                                          Routing r) {
+  __shared__ float part[8][kSmallT];
+  __shared__ int ids_s[kSmallT * kMaxTopK];
+  __shared__ int counts_s[kMaxExperts];
+  __shared__ int offs_s[kMaxExperts];
+  __shared__ int scratch[16];
+  __shared__ float lbuf[8][kMaxExperts];
+  __shared__ unsigned last;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = blockIdx.x * 2 + (warp >> 2);
+  const int q = warp & 3;
+  const int kq = d.H / 4;  // K range of one warp
+
+  // interleaved copy of x for the expert GEMV operand (grid-stride, 16 B)
+  {
+    const int chunks = d.T * d.H / 8;
+    const uint4* src = reinterpret_cast<const uint4*>(x);
+    uint4* dst = reinterpret_cast<uint4*>(xg);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < chunks; i += gridDim.x * blockDim.x)
+      dst[i] = interleave8(src[i]);
+  }
+
+  if (e < d.E) {
+    const float4* wrow = reinterpret_cast<const float4*>(router_w + (size_t)e * d.H + q * kq);
+    const int nf = kq / 4;  // float4 per warp
+    for (int t = 0; t < d.T; ++t) {
+      const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)t * d.H + q * kq);
+      float acc = 0.f;
+      for (int f0 = 0; f0 < nf; f0 += 32 * 4) {
+        float4 wv[4];
+        uint2 xv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int f = f0 + u * 32 + lane;
+          if (f < nf) {
+            wv[u] = __ldg(wrow + f);
+            xv[u] = __ldg(xr + f);
+          } else {
+            wv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            xv[u] = make_uint2(0u, 0u);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          acc = fmaf(__uint_as_float(xv[u].x << 16), wv[u].x, acc);
+          acc = fmaf(__uint_as_float(xv[u].x & 0xffff0000u), wv[u].y, acc);
+          acc = fmaf(__uint_as_float(xv[u].y << 16), wv[u].z, acc);
+          acc = fmaf(__uint_as_float(xv[u].y & 0xffff0000u), wv[u].w, acc);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) part[warp][t] = acc;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < 2 * d.T) {
+    const int sub = threadIdx.x / d.T, t = threadIdx.x % d.T;
+    const int ee = blockIdx.x * 2 + sub;
+    if (ee < d.E) {
+      const float v = ((part[4 * sub][t] + part[4 * sub + 1][t]) + part[4 * sub + 2][t]) +
+                      part[4 * sub + 3][t];
+      r.logits[(size_t)t * d.E + ee] = v;
+    }
+  }
+
+  // ---- last CTA finishes routing for all tokens
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = (atomicAdd(&r.tickets[kTicketRouter], 1u) == gridDim.x - 1);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+
+  for (int i = threadIdx.x; i < d.E; i += blockDim.x) counts_s[i] = 0;
+  __syncthreads();
+  for (int t = warp; t < d.T; t += 8) {
+    const float* lrow = r.logits + (size_t)t * d.E;
+    int id;
+    float w;
+    // logits were written by other CTAs: read through L2
+    float lv[kMaxExperts / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int ee = lane + 32 * i;
+      lv[i] = (ee < d.E) ? __ldcg(lrow + ee) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int ee = lane + 32 * i;
+      if (ee < d.E) lbuf[warp][ee] = lv[i];
+    }
+    __syncwarp();
+    warp_topk(lbuf[warp], bias, d.E, d.k, lane, &id, &w);
+    __syncwarp();
+    if (lane < d.k) {
+      if (id < 0 || id >= d.E) {
+        atomicOr(r.err, kErrRange);
+        id = 0;
+      }
+      r.ids[t * d.k + lane] = id;
+      r.wts[t * d.k + lane] = w;
+      ids_s[t * d.k + lane] = id;
+      atomicAdd(&counts_s[id], 1);
+    }
+  }
+  __syncthreads();
+  int total;
+  {
+    const int c = (threadIdx.x < d.E) ? counts_s[threadIdx.x] : 0;
+    const int ex = block_scan_256(c, scratch, &total);
+    if (threadIdx.x < d.E) {
+      offs_s[threadIdx.x] = ex;
+      r.offsets[threadIdx.x] = ex;
+      r.counts[threadIdx.x] = c;
+    }
+    if (threadIdx.x == 0) r.offsets[d.E] = total;
+  }
+  __syncthreads();
+  // stable placement: rank of item i among earlier items with the same expert
+  const int n = d.T * d.k;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int ei = ids_s[i];
+    int rank = 0;
+    for (int j = 0; j < i; ++j) rank += (ids_s[j] == ei);
+    const int pos = offs_s[ei] + rank;
+    r.perm[pos] = i / d.k;
+    r.inv[i] = pos;
+  }
+  build_task_lists(d, counts_s, r, scratch);
+  if (threadIdx.x == 0) r.tickets[kTicketRouter] = 0u;
+}
+
+// ----------------------------------------------------------------- large T
+// logits[T, E] = x[T, H] . Wr[E, H]^T in fp32: 64x64 tiles, K chunks of 32,
+// 4x4 outputs per thread. Also writes the interleaved copy of x.
+__global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ x,
+                                                            const float* __restrict__ router_w,
+                                                            uint16_t* __restrict__ xg, Dims d,
+                                                            Routing r) {
+  __shared__ float xs[32][64 + 4];
+  __shared__ float ws[32][64 + 4];
+  const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+
+  if (blockIdx.y == 0) {
+    const int rows = min(64, d.T - t0);
+    const int chunks = rows * d.H / 8;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t0 * d.H);
+    uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)t0 * d.H);
+    for (int i = threadIdx.x; i < chunks; i += blockDim.x) dst[i] = interleave8(src[i]);
+  }
+
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < d.H; k0 += 32) {
+    // load 64 tokens x 32 k of x (bf16 -> f32) and 64 experts x 32 k of Wr
+    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
+      const int row = i >> 5, kk = i & 31;
+      const int t = t0 + row, ee = e0 + row;
+      xs[kk][row] = (t < d.T) ? bf16_bits_to_f32(x[(size_t)t * d.H + k0 + kk]) : 0.f;
+      ws[kk][row] = (ee < d.E) ? router_w[(size_t)ee * d.H + k0 + kk] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < 32; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[i] = xs[kk][ty * 4 + i];
+        b[i] = ws[kk][tx * 4 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= d.T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int ee = e0 + tx * 4 + j;
+      if (ee < d.E) r.logits[(size_t)t * d.E + ee] = acc[i][j];
+    }
+  }
+}
+
+// Top-k for kTopkTokens tokens per CTA (8 warps), CTA expert histogram; the
+// last CTA computes counts, offsets, each CTA's first row per expert and the
+// task lists.
+__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ bias, Dims d,
+                                                          Routing r) {
+  __shared__ int hist[kMaxExperts];
+  __shared__ int counts_s[kMaxExperts];
+  __shared__ int scratch[16];
+  __shared__ unsigned last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kMaxExperts; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int t0 = blockIdx.x * kTopkTokens;
+  for (int t = t0 + warp; t < min(d.T, t0 + kTopkTokens); t += 8) {
+    int id;
+    float w;
+    warp_topk(r.logits + (size_t)t * d.E, bias, d.E, d.k, lane, &id, &w);
+    if (lane < d.k) {
+      if (id < 0 || id >= d.E) {
+        atomicOr(r.err, kErrRange);
+        id = 0;
+      }
+      r.ids[t * d.k + lane] = id;
+      r.wts[t * d.k + lane] = w;
+      atomicAdd(&hist[id], 1);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < d.E; i += blockDim.x)
+    r.blockcnt[(size_t)blockIdx.x * d.E + i] = hist[i];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = (atomicAdd(&r.tickets[kTicketTopk], 1u) == gridDim.x - 1);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const int nblk = gridDim.x;
+  const int e = threadIdx.x;
+  int c = 0;
+  if (e < d.E)
+    for (int b = 0; b < nblk; ++b) c += __ldcg(r.blockcnt + (size_t)b * d.E + e);
+  int total;
+  const int ex = block_scan_256(c, scratch, &total);
+  if (e < d.E) {
+    counts_s[e] = c;
+    r.counts[e] = c;
+    r.offsets[e] = ex;
+    int run = ex;
+    for (int b = 0; b < nblk; ++b) {
+      r.blockbase[(size_t)b * d.E + e] = run;
+      run += __ldcg(r.blockcnt + (size_t)b * d.E + e);
+    }
+  }
+  if (threadIdx.x == 0) r.offsets[d.E] = total;
+  __syncthreads();
+  build_task_lists(d, counts_s, r, scratch);
+  if (threadIdx.x == 0) r.tickets[kTicketTopk] = 0u;
+}
+
+// Stable placement of one CTA's items (tokens [t0, t0 + kTopkTokens), items in
+// (token, slot) order). Items are ranked chunk by chunk: within a warp by
+// __match_any_sync, across warps by a per-warp count table.
+__global__ void __launch_bounds__(256) route_place_kernel(Dims d, Routing r) {
+  __shared__ int run[kMaxExperts];
+  __shared__ int wcnt[8][kMaxExperts];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < d.E; i += blockDim.x)
+    run[i] = r.blockbase[(size_t)blockIdx.x * d.E + i];
+  for (int i = threadIdx.x; i < 8 * kMaxExperts; i += blockDim.x) (&wcnt[0][0])[i] = 0;
+  __syncthreads();
+  const int i0 = blockIdx.x * kTopkTokens * d.k;
+  const int i1 = min(d.T, (blockIdx.x + 1) * kTopkTokens) * d.k;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int c0 = i0; c0 < i1; c0 += 256) {
+    const int i = c0 + threadIdx.x;
+    const bool valid = i < i1;
+    int e = valid ? r.ids[i] : -1;
+    if (valid && (e < 0 || e >= d.E)) {
+      atomicOr(r.err, kErrRange);
+      e = 0;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt);
+    if (valid && rank == 0) wcnt[warp][e] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+      int pos = run[e] + rank;
+      for (int w = 0; w < warp; ++w) pos += wcnt[w][e];
+      r.perm[pos] = i / d.k;
+      r.inv[i] = pos;
+    }
+    __syncthreads();
+    for (int ee = threadIdx.x; ee < d.E; ee += blockDim.x) {
+      int s = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        s += wcnt[w][ee];
+        wcnt[w][ee] = 0;
+      }
+      run[ee] += s;
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ launcher
+cudaError_t launch_route(const Dims& d, const Routing& r, const uint16_t* x, const float* router_w,
+                         const float* bias, uint16_t* xg, cudaStream_t s, LaunchLog& log) {
+  if (d.T <= kSmallT) {
+    log.begin("route_small", s);
+    route_small_kernel<<<(d.E + 1) / 2, 256, 0, s>>>(x, router_w, bias, xg, d, r);
+    log.end(s);
+    return cudaGetLastError();
+  }
+  const int nblk = (d.T + kTopkTokens - 1) / kTopkTokens;
+  log.begin("router_logits", s);
+  router_logits_kernel<<<dim3((d.T + 63) / 64, (d.E + 63) / 64), 256, 0, s>>>(x, router_w, xg, d, r);
+  log.end(s);
+  log.begin("router_topk", s);
+  router_topk_kernel<<<nblk, 256, 0, s>>>(bias, d, r);
+  log.end(s);
+  log.begin("route_place", s);
+  route_place_kernel<<<nblk, 256, 0, s>>>(d, r);
+  log.end(s);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
