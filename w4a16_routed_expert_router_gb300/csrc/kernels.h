@@ -7,10 +7,10 @@ namespace moe {
 
 constexpr int kSmallT = 64;       // <= this many tokens: single-kernel router
 constexpr int kTopkTokens = 64;   // tokens per CTA in the large-T router
-constexpr int kPassRows = 16;     // expert rows per GEMV task (two 8-token MMA blocks)
+constexpr int kPassRows = 8;      // expert rows per GEMV task (one 8-column MMA block)
 constexpr int kTile1 = 16;        // gate (and up) channels per gate/up GEMV task
 constexpr int kTile2 = 32;        // output channels per down GEMV task
-constexpr int kGemvStages = 8;    // TMA pipeline depth of the GEMV kernels
+constexpr int kGemvStages = 6;    // TMA pipeline depth of the GEMV kernels
 constexpr int kGemvThreads = 288; // 8 consumer warps + 1 TMA producer warp
 
 // Records the kernels one forward launches (and their CUDA events when
@@ -38,20 +38,24 @@ struct LaunchLog {
 struct GemvWeights {
   const uint16_t* scale_routed;
   const uint16_t* scale_shared;
-  CUtensorMap tm_routed;
+  CUtensorMap tm_routed;   // packed INT4 weights, 3-D view (see encode_int4_map)
   CUtensorMap tm_shared;
+  CUtensorMap ts_routed;   // bf16 group scales, 2-D view, when scale_tma
+  CUtensorMap ts_shared;
+  int scale_tma;           // K / 128 is a multiple of 8: scales ride in the TMA stage
 };
 
 cudaError_t launch_route(const Dims& d, const Routing& r, const uint16_t* x, const float* router_w,
-                         const float* bias, uint16_t* xg, cudaStream_t s, LaunchLog& log);
+                         const float* bias, cudaStream_t s, LaunchLog& log);
 
 cudaError_t gemv_setup(int* ctas_per_sm);
 cudaError_t launch_gemv_gate_up(const Dims& d, const Routing& r, const GemvWeights& w,
-                                const uint16_t* xg, uint16_t* h, int hstride, int grid,
+                                const uint16_t* x, uint16_t* h, int hstride, int grid,
                                 cudaStream_t s, LaunchLog& log);
+// out != nullptr: fuse the combine (small batches); else only y is written.
 cudaError_t launch_gemv_down(const Dims& d, const Routing& r, const GemvWeights& w,
-                             const uint16_t* h, int hstride, float* y, int grid, cudaStream_t s,
-                             LaunchLog& log);
+                             const uint16_t* h, int hstride, float* y, uint16_t* out,
+                             int* tile_cnt, int grid, cudaStream_t s, LaunchLog& log);
 cudaError_t launch_combine(const Dims& d, const Routing& r, const float* y, uint16_t* out,
                            cudaStream_t s, LaunchLog& log);
 

@@ -18,7 +18,7 @@ struct moe_w4a16_handle {
   void* ws = nullptr;
   size_t ws_bytes = 0;
   Routing r{};
-  uint16_t* xg = nullptr;
+  int* tile_cnt = nullptr;      // [H / 32] combine tickets of the down kernel
   uint16_t* h = nullptr;
   int hstride = 0;
   float* y = nullptr;
@@ -28,9 +28,10 @@ struct moe_w4a16_handle {
   LaunchLog log;
   cudaEvent_t events[2 * LaunchLog::kMax];
   bool events_made = false;
-  // tensor-map cache keyed by the weight pointers it was encoded for
-  const void* map_keys[4] = {nullptr, nullptr, nullptr, nullptr};
-  CUtensorMap maps[4];
+  // tensor-map cache keyed by the tensor pointers it was encoded for:
+  // 0 w13_q, 1 w2_q, 2 sh_w13_q, 3 sh_w2_q, 4 w13_s, 5 w2_s, 6 sh_w13_s, 7 sh_w2_s
+  const void* map_keys[8] = {};
+  CUtensorMap maps[8];
 };
 
 namespace {
@@ -106,7 +107,7 @@ Layout plan(const moe_w4a16_config& c) {
       nblk * E * 4,          // 12 blockbase
       kTickets * 4,          // 13 tickets
       4,                     // 14 err
-      Tm * H * 2,            // 15 xg
+      (size_t)H / 32 * 4,    // 15 tile_cnt
       rows * hstride * 2,    // 16 h
       rows * H * 4,          // 17 y
       Tm * H * 2,            // 18 x_dev
@@ -147,9 +148,30 @@ int encode_int4_map(CUtensorMap* m, const void* base, long long rows, int K) {
   return MOE_W4A16_OK;
 }
 
+// 2-D view {K/128 groups, rows} of bf16 group scales [rows, K/128], box
+// {8, 16}: 8 groups of 16 rows. Needs K/128 to be a multiple of 8 (16-byte
+// row stride).
+int encode_scale_map(CUtensorMap* m, const void* base, long long rows, int K) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MOE_W4A16_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)(K / kGroup), (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(K / kGroup) * 2};
+  cuuint32_t box[2] = {8, 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    fprintf(stderr, "moe_w4a16: cuTensorMapEncodeTiled (scales) failed (%d)\n", (int)r);
+    return MOE_W4A16_ERR_CUDA;
+  }
+  return MOE_W4A16_OK;
+}
+
 int get_map(moe_w4a16_handle* h, int slot, const void* base, long long rows, int K) {
   if (h->map_keys[slot] == base && base) return MOE_W4A16_OK;
-  const int st = encode_int4_map(&h->maps[slot], base, rows, K);
+  const int st = slot < 4 ? encode_int4_map(&h->maps[slot], base, rows, K)
+                          : encode_scale_map(&h->maps[slot], base, rows, K);
   if (st == MOE_W4A16_OK) h->map_keys[slot] = base;
   return st;
 }
@@ -249,7 +271,7 @@ int moe_w4a16_create(const moe_w4a16_config* cfg, int device, moe_w4a16_handle**
   r.blockbase = reinterpret_cast<int*>(b + L.off[12]);
   r.tickets = reinterpret_cast<unsigned*>(b + L.off[13]);
   r.err = reinterpret_cast<unsigned*>(b + L.off[14]);
-  h->xg = reinterpret_cast<uint16_t*>(b + L.off[15]);
+  h->tile_cnt = reinterpret_cast<int*>(b + L.off[15]);
   h->h = reinterpret_cast<uint16_t*>(b + L.off[16]);
   h->hstride = cfg->inter > cfg->shared_inter ? cfg->inter : cfg->shared_inter;
   h->y = reinterpret_cast<float*>(b + L.off[17]);
@@ -305,35 +327,54 @@ int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t T, const m
   if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) cudaSetDevice(h->device);
 
   Dims d{T, c.hidden, c.num_experts, c.top_k, c.inter, c.shared_inter};
-  // tensor maps (cached per weight pointer)
-  GemvWeights g1, g2;
-  if ((st = get_map(h, 0, w->w13_q, (long long)c.num_experts * 2 * c.inter, c.hidden)) != MOE_W4A16_OK)
-    return st;
-  if ((st = get_map(h, 1, w->w2_q, (long long)c.num_experts * c.hidden, c.inter)) != MOE_W4A16_OK)
-    return st;
-  if (c.shared_inter > 0) {
+  const bool has_sh = c.shared_inter > 0;
+  // scales ride in the TMA stages when every K has a multiple of 8 groups
+  const bool scale_tma = (c.hidden / kGroup) % 8 == 0 && (c.inter / kGroup) % 8 == 0 &&
+                         (!has_sh || (c.shared_inter / kGroup) % 8 == 0);
+  const long long r13 = (long long)c.num_experts * 2 * c.inter, r2 = (long long)c.num_experts * c.hidden;
+  if ((st = get_map(h, 0, w->w13_q, r13, c.hidden)) != MOE_W4A16_OK) return st;
+  if ((st = get_map(h, 1, w->w2_q, r2, c.inter)) != MOE_W4A16_OK) return st;
+  if (has_sh) {
     if ((st = get_map(h, 2, w->sh_w13_q, 2LL * c.shared_inter, c.hidden)) != MOE_W4A16_OK) return st;
     if ((st = get_map(h, 3, w->sh_w2_q, c.hidden, c.shared_inter)) != MOE_W4A16_OK) return st;
   }
+  if (scale_tma) {
+    if ((st = get_map(h, 4, w->w13_s, r13, c.hidden)) != MOE_W4A16_OK) return st;
+    if ((st = get_map(h, 5, w->w2_s, r2, c.inter)) != MOE_W4A16_OK) return st;
+    if (has_sh) {
+      if ((st = get_map(h, 6, w->sh_w13_s, 2LL * c.shared_inter, c.hidden)) != MOE_W4A16_OK)
+        return st;
+      if ((st = get_map(h, 7, w->sh_w2_s, c.hidden, c.shared_inter)) != MOE_W4A16_OK) return st;
+    }
+  }
+  GemvWeights g1, g2;
   g1.tm_routed = h->maps[0];
-  g1.tm_shared = c.shared_inter > 0 ? h->maps[2] : h->maps[0];
+  g1.tm_shared = has_sh ? h->maps[2] : h->maps[0];
+  g1.ts_routed = scale_tma ? h->maps[4] : h->maps[0];
+  g1.ts_shared = scale_tma && has_sh ? h->maps[6] : g1.ts_routed;
   g1.scale_routed = w->w13_s;
-  g1.scale_shared = c.shared_inter > 0 ? w->sh_w13_s : w->w13_s;
+  g1.scale_shared = has_sh ? w->sh_w13_s : w->w13_s;
+  g1.scale_tma = scale_tma;
   g2.tm_routed = h->maps[1];
-  g2.tm_shared = c.shared_inter > 0 ? h->maps[3] : h->maps[1];
+  g2.tm_shared = has_sh ? h->maps[3] : h->maps[1];
+  g2.ts_routed = scale_tma ? h->maps[5] : h->maps[1];
+  g2.ts_shared = scale_tma && has_sh ? h->maps[7] : g2.ts_routed;
   g2.scale_routed = w->w2_s;
-  g2.scale_shared = c.shared_inter > 0 ? w->sh_w2_s : w->w2_s;
+  g2.scale_shared = has_sh ? w->sh_w2_s : w->w2_s;
+  g2.scale_tma = scale_tma;
 
+  const bool fuse = T <= kSmallT;
   cudaError_t e;
-  if ((e = launch_route(d, h->r, x, w->router_w, w->router_bias, h->xg, s, h->log)) != cudaSuccess)
+  if ((e = launch_route(d, h->r, x, w->router_w, w->router_bias, s, h->log)) != cudaSuccess)
     return cuda_status(e);
-  if ((e = launch_gemv_gate_up(d, h->r, g1, h->xg, h->h, h->hstride, h->gemv_grid, s, h->log)) !=
+  if ((e = launch_gemv_gate_up(d, h->r, g1, x, h->h, h->hstride, h->gemv_grid, s, h->log)) !=
       cudaSuccess)
     return cuda_status(e);
-  if ((e = launch_gemv_down(d, h->r, g2, h->h, h->hstride, h->y, h->gemv_grid, s, h->log)) !=
-      cudaSuccess)
+  if ((e = launch_gemv_down(d, h->r, g2, h->h, h->hstride, h->y, fuse ? out : nullptr,
+                            h->tile_cnt, h->gemv_grid, s, h->log)) != cudaSuccess)
     return cuda_status(e);
-  if ((e = launch_combine(d, h->r, h->y, out, s, h->log)) != cudaSuccess) return cuda_status(e);
+  if (!fuse)
+    if ((e = launch_combine(d, h->r, h->y, out, s, h->log)) != cudaSuccess) return cuda_status(e);
   h->last_T = T;
   return MOE_W4A16_OK;
 }

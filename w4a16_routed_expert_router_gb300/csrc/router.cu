@@ -114,47 +114,35 @@ __device__ __forceinline__ int block_scan_256(int v, int* scratch /* >= 8 ints *
   return base + inc - v;
 }
 
-// Active-expert list and task prefixes, run by one 256-thread block after the
-// counts are final. counts_s: shared [E]. Writes active/task1/task2/meta.
+// Active routed experts (ascending) and the prefix of their expert-kernel
+// tasks, run by one 256-thread block once counts_s (shared [E]) is final.
+// The shared expert's tasks are not listed: the expert kernels put them first.
 __device__ void build_task_lists(const Dims& d, const int* counts_s, const Routing& r,
                                  int* scratch) {
   const int e = threadIdx.x;
   const int c = (e < d.E) ? counts_s[e] : 0;
   int n_act;
   const int idx = block_scan_256(c > 0 ? 1 : 0, scratch, &n_act);
-  if (e < d.E && c > 0) r.active[idx] = e;
-  const int n_total = n_act + (d.Is > 0 ? 1 : 0);
-  if (threadIdx.x == 0 && d.Is > 0) r.active[n_act] = d.E;
-  __syncthreads();
-  // task prefix: a < n_total <= 257 entries, one per thread (+ one extra)
-  int tot1 = 0, tot2 = 0;
-  for (int base = 0; base < n_total; base += 256) {
-    const int a = base + threadIdx.x;
-    int c1 = 0, c2 = 0;
-    if (a < n_total) {
-      const int ex = r.active[a];
-      const bool sh = (ex == d.E);
-      const int rows = sh ? d.T : counts_s[ex];
-      const int p = passes_for(rows);
-      c1 = p * ((sh ? d.Is : d.I) / kTile1);
-      c2 = p * (d.H / kTile2);
-    }
-    int s1, s2;
-    const int x1 = block_scan_256(c1, scratch, &s1);
-    const int x2 = block_scan_256(c2, scratch, &s2);
-    if (a < n_total) {
-      r.task1[a] = tot1 + x1;
-      r.task2[a] = tot2 + x2;
-    }
-    tot1 += s1;
-    tot2 += s2;
+  int c1 = 0, c2 = 0;
+  if (e < d.E && c > 0) {
+    const int p = passes_for(c);
+    c1 = p * (d.I / kTile1);
+    c2 = p * (d.H / kTile2);
+  }
+  int s1, s2;
+  const int x1 = block_scan_256(c1, scratch, &s1);
+  const int x2 = block_scan_256(c2, scratch, &s2);
+  if (e < d.E && c > 0) {
+    r.active[idx] = e;
+    r.task1[idx] = x1;
+    r.task2[idx] = x2;
   }
   if (threadIdx.x == 0) {
-    r.task1[n_total] = tot1;
-    r.task2[n_total] = tot2;
-    r.meta[kMetaActive] = n_total;
-    r.meta[kMetaTasks1] = tot1;
-    r.meta[kMetaTasks2] = tot2;
+    r.task1[n_act] = s1;
+    r.task2[n_act] = s2;
+    r.meta[kMetaActive] = n_act;
+    r.meta[kMetaTasks1] = s1;
+    r.meta[kMetaTasks2] = s2;
   }
 }
 
@@ -165,8 +153,7 @@ __device__ void build_task_lists(const Dims& d, const int* counts_s, const Routi
 // expert 2b+1, each warp a quarter of H. Requires T <= kSmallT, H % 512 == 0.
 __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __restrict__ x,
                                                           const float* __restrict__ router_w,
-                                                          const float* __restrict__ bias,
-                                                          uint16_t* __restrict__ xg, Dims d,
+                                                          const float* __restrict__ bias, Dims d,
                                                           Routing r) {
   __shared__ float part[8][kSmallT];
   __shared__ int ids_s[kSmallT * kMaxTopK];
@@ -181,14 +168,8 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
   const int q = warp & 3;
   const int kq = d.H / 4;  // K range of one warp
 
-  // interleaved copy of x for the expert GEMV operand (grid-stride, 16 B)
-  {
-    const int chunks = d.T * d.H / 8;
-    const uint4* src = reinterpret_cast<const uint4*>(x);
-    uint4* dst = reinterpret_cast<uint4*>(xg);
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < chunks; i += gridDim.x * blockDim.x)
-      dst[i] = interleave8(src[i]);
-  }
+  // let the expert kernel start its shared-expert work right away
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (e < d.E) {
     const float4* wrow = reinterpret_cast<const float4*>(router_w + (size_t)e * d.H + q * kq);
@@ -196,11 +177,11 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
     for (int t = 0; t < d.T; ++t) {
       const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)t * d.H + q * kq);
       float acc = 0.f;
-      for (int f0 = 0; f0 < nf; f0 += 32 * 4) {
-        float4 wv[4];
-        uint2 xv[4];
+      for (int f0 = 0; f0 < nf; f0 += 32 * 8) {
+        float4 wv[8];
+        uint2 xv[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 8; ++u) {
           const int f = f0 + u * 32 + lane;
           if (f < nf) {
             wv[u] = __ldg(wrow + f);
@@ -211,7 +192,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
           }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 8; ++u) {
           acc = fmaf(__uint_as_float(xv[u].x << 16), wv[u].x, acc);
           acc = fmaf(__uint_as_float(xv[u].x & 0xffff0000u), wv[u].y, acc);
           acc = fmaf(__uint_as_float(xv[u].y << 16), wv[u].z, acc);
@@ -303,23 +284,14 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
 
 // ----------------------------------------------------------------- large T
 // logits[T, E] = x[T, H] . Wr[E, H]^T in fp32: 64x64 tiles, K chunks of 32,
-// 4x4 outputs per thread. Also writes the interleaved copy of x.
+// 4x4 outputs per thread.
 __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ x,
                                                             const float* __restrict__ router_w,
-                                                            uint16_t* __restrict__ xg, Dims d,
-                                                            Routing r) {
+                                                            Dims d, Routing r) {
   __shared__ float xs[32][64 + 4];
   __shared__ float ws[32][64 + 4];
   const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-
-  if (blockIdx.y == 0) {
-    const int rows = min(64, d.T - t0);
-    const int chunks = rows * d.H / 8;
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t0 * d.H);
-    uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)t0 * d.H);
-    for (int i = threadIdx.x; i < chunks; i += blockDim.x) dst[i] = interleave8(src[i]);
-  }
 
   float acc[4][4] = {};
   for (int k0 = 0; k0 < d.H; k0 += 32) {
@@ -465,16 +437,16 @@ __global__ void __launch_bounds__(256) route_place_kernel(Dims d, Routing r) {
 
 // ------------------------------------------------------------------ launcher
 cudaError_t launch_route(const Dims& d, const Routing& r, const uint16_t* x, const float* router_w,
-                         const float* bias, uint16_t* xg, cudaStream_t s, LaunchLog& log) {
+                         const float* bias, cudaStream_t s, LaunchLog& log) {
   if (d.T <= kSmallT) {
     log.begin("route_small", s);
-    route_small_kernel<<<(d.E + 1) / 2, 256, 0, s>>>(x, router_w, bias, xg, d, r);
+    route_small_kernel<<<(d.E + 1) / 2, 256, 0, s>>>(x, router_w, bias, d, r);
     log.end(s);
     return cudaGetLastError();
   }
   const int nblk = (d.T + kTopkTokens - 1) / kTopkTokens;
   log.begin("router_logits", s);
-  router_logits_kernel<<<dim3((d.T + 63) / 64, (d.E + 63) / 64), 256, 0, s>>>(x, router_w, xg, d, r);
+  router_logits_kernel<<<dim3((d.T + 63) / 64, (d.E + 63) / 64), 256, 0, s>>>(x, router_w, d, r);
   log.end(s);
   log.begin("router_topk", s);
   router_topk_kernel<<<nblk, 256, 0, s>>>(bias, d, r);
