@@ -11,17 +11,18 @@
 //    (expert, channel tile, pass of <= 8 rows of that expert's segment). The
 //    shared expert's tasks come first: they need no routing, so with
 //    programmatic dependent launch they start while the router still runs.
-//  * one producer thread fills a 6-stage shared-memory ring: per stage 3-D TMA
-//    loads of two 16-row weight tiles x 8 K-groups of 128 (16 KB of INT4), a
-//    2-D TMA load of their bf16 group scales, and 1-D bulk copies of the
-//    matching activation chunk of every row of the pass (x for gate/up, h for
-//    down), all counted on one mbarrier.
+//  * one producer warp decodes the tasks (from a shared-memory copy of the
+//    routing metadata) and fills a 6-stage ring: per stage 3-D TMA loads of two
+//    16-row weight tiles x 8 K-groups of 128 (16 KB of INT4), a 2-D TMA load of
+//    their bf16 group scales, and 1-D bulk copies of the matching activation
+//    chunk of every row of the pass (x for gate/up, h for down), all counted
+//    on one mbarrier, plus a stage descriptor telling the consumers what the
+//    stage holds.
 //  * 8 consumer warps split K: warp w takes K-group w of every stage. Each
-//    lane turns its 4-bit codes into exact bf16 integers (lop3 into the bf16
-//    mantissa, one bf16x2 subtract) and feeds mma.sync m16n8k16 with weights as
-//    the 16-row A operand and the pass's (up to 8) rows as B. The group scale
-//    is applied in fp32 to the group's partial sums, so q * scale is never
-//    rounded.
+//    lane turns its 4-bit codes into exact bf16 integers and feeds mma.sync
+//    m16n8k16 with weights as the 16-row A operand and the pass's rows as B.
+//    The group scale is applied in fp32 to the group's partial sums, so
+//    q * scale is never rounded.
 //  * the K order inside one MMA is a fixed permutation of the true K order;
 //    the activation operand is put in the same order ("interleaved": within
 //    each 8 values (0,4)(1,5)(2,6)(3,7)): x in registers, h by the gate/up
@@ -30,6 +31,8 @@
 //    invariant); gate/up epilogue SwiGLU -> bf16 h; down epilogue fp32 y and,
 //    for small batches, the combine: the last task to finish a channel tile
 //    (atomic ticket, no waiting) writes out = y_shared + sum_j w_j y_j there.
+//  * every wait is an mbarrier wait bounded in time (no named barriers), so a
+//    broken hand-off ends the kernel with an error flag instead of a hang.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -43,8 +46,29 @@ constexpr int kSBytes = 2 * 16 * 8 * 2;            // 2 tiles x 16 rows x 8 grou
 constexpr int kXStride = 8 * 256 + 64;             // one row's 8 groups (bf16) + pad
 constexpr int kXOff = kWBytes + kSBytes;
 constexpr int kStageBytes = ((kXOff + kRows * kXStride) + 1023) / 1024 * 1024;
-constexpr int kRedBytes = 8 * 2 * 32 * 16;         // warps x tiles x lanes x float4
-constexpr int kSmemBytes = kGemvStages * kStageBytes + kRedBytes + 2 * kGemvStages * 8 + 16;
+
+enum DescFlags { kFirst = 1, kLast = 2, kEnd = 4, kShared = 8 };
+
+// What one stage holds; written by the producer before the stage's arrive.
+struct Desc {
+  int flags, g0, gcnt, ngroups, tile, r0, nr, rowA0, rowA1, pad[3];
+};
+
+enum Bar { kBarRedFull = 0, kBarRedEmpty, kBarYDone, kBarFlag, kNumBars };
+
+struct Smem {
+  uint8_t stage[kGemvStages][kStageBytes];
+  float4 red[8 * 2 * 32];
+  Desc desc[kGemvStages];
+  int active[kMaxExperts + 2];
+  int prefix[kMaxExperts + 2];
+  int offsets[kMaxExperts + 2];
+  uint64_t full[kGemvStages];
+  uint64_t empty[kGemvStages];
+  uint64_t bar[kNumBars];
+  int flag;
+};
+constexpr int kSmemBytes = (int)sizeof(Smem);
 
 struct GemvParams {
   Dims d;
@@ -79,15 +103,11 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 __device__ __forceinline__ int passes_of(int rows) { return (rows + kRows - 1) / kRows; }
 
-template <int MODE>
-__device__ __forceinline__ int tiles_of(const Dims& d, bool shared) {
-  return MODE == 1 ? (shared ? d.Is : d.I) / kTile1 : d.H / kTile2;
-}
-
 // Tasks of the shared expert: they come first and need no routing.
 template <int MODE>
 __device__ __forceinline__ int shared_tasks(const Dims& d) {
-  return d.Is > 0 ? tiles_of<MODE>(d, true) * passes_of(d.T) : 0;
+  if (d.Is == 0) return 0;
+  return (MODE == 1 ? d.Is / kTile1 : d.H / kTile2) * passes_of(d.T);
 }
 
 template <int MODE>
@@ -113,36 +133,20 @@ __device__ __forceinline__ Task make_task(const Dims& d, bool shared, int e, int
   return t;
 }
 
+// Routed task tau (counted after the shared ones), decoded from the
+// shared-memory copy of the active-expert list and its task prefix.
 template <int MODE>
-__device__ __forceinline__ Task shared_task(const Dims& d, int tau) {
-  return make_task<MODE>(d, true, d.E, d.T * d.k, d.T * d.k + d.T, tau);
-}
-
-// Routed task tau (counted after the shared ones): binary search of the
-// active expert whose task range holds tau.
-template <int MODE>
-__device__ __forceinline__ Task routed_task(const GemvParams& p, int tau) {
-  const int* prefix = (MODE == 1) ? p.r.task1 : p.r.task2;
-  const int n_act = p.r.meta[kMetaActive];
+__device__ __forceinline__ Task routed_task(const Smem& s, const Dims& d, int n_act, int tau) {
   int lo = 0, hi = n_act - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(prefix + mid) <= tau)
+    if (s.prefix[mid] <= tau)
       lo = mid;
     else
       hi = mid - 1;
   }
-  const int e = __ldg(p.r.active + lo);
-  return make_task<MODE>(p.d, false, e, __ldg(p.r.offsets + e), __ldg(p.r.offsets + e + 1),
-                         tau - __ldg(prefix + lo));
-}
-
-// Activation row of expert-sorted row r: a token of x (gate/up) or a row of h.
-template <int MODE>
-__device__ __forceinline__ const uint16_t* act_row(const GemvParams& p, const Task& t, int r) {
-  int row = r;
-  if (MODE == 1) row = t.shared ? r - p.d.T * p.d.k : __ldg(p.r.perm + r);
-  return p.bsrc + (size_t)row * p.bstride;
+  const int e = s.active[lo];
+  return make_task<MODE>(d, false, e, s.offsets[e], s.offsets[e + 1], tau - s.prefix[lo]);
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -177,10 +181,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-__device__ __forceinline__ void named_bar_consumers() {
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-}
-
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
   return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
 }
@@ -211,32 +211,12 @@ __device__ __forceinline__ void group_mma(const uint4& wA, const uint4& wB, cons
   for (int i = 0; i < 4; ++i) out[i] = t0[i] + t1[i];
 }
 
+// Activation row of expert-sorted row r: a token of x (gate/up) or a row of h.
 template <int MODE>
-__device__ __forceinline__ uint32_t stage_bytes(const Task& t, int gcnt, bool scale_tma) {
-  return gcnt * 2 * 1024 + (scale_tma ? kSBytes : 0) + t.nr * gcnt * 256;
-}
-
-// Producer: weights and scales of one stage (no dependency on earlier kernels).
-__device__ __forceinline__ void issue_weights(uint8_t* st, uint64_t* bar, const CUtensorMap* tm,
-                                              const CUtensorMap* ts, const Task& t, int g0,
-                                              int gcnt, bool scale_tma) {
-  for (int g = 0; g < gcnt; ++g) {
-    tma_load_3d(st + g * 1024, tm, bar, 0, g0 + g, t.rowA0);
-    tma_load_3d(st + (8 + g) * 1024, tm, bar, 0, g0 + g, t.rowA1);
-  }
-  if (scale_tma) {
-    tma_load_2d(smem_u32(st + kWBytes), ts, bar, g0, t.rowA0);
-    tma_load_2d(smem_u32(st + kWBytes + 256), ts, bar, g0, t.rowA1);
-  }
-}
-
-// Producer: activation chunks of one stage (depends on earlier kernels).
-template <int MODE>
-__device__ __forceinline__ void issue_acts(const GemvParams& p, uint8_t* st, uint64_t* bar,
-                                           const Task& t, int g0, int gcnt) {
-  for (int j = 0; j < t.nr; ++j)
-    bulk_copy(smem_u32(st + kXOff + j * kXStride), act_row<MODE>(p, t, t.r0 + j) + g0 * kGroup,
-              gcnt * 256, bar);
+__device__ __forceinline__ const uint16_t* act_row(const GemvParams& p, const Task& t, int r) {
+  int row = r;
+  if (MODE == 1) row = t.shared ? r - p.d.T * p.d.k : __ldg(p.r.perm + r);
+  return p.bsrc + (size_t)row * p.bstride;
 }
 
 template <int MODE>
@@ -245,200 +225,211 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                 const __grid_constant__ CUtensorMap tm_shared,
                 const __grid_constant__ CUtensorMap ts_routed,
                 const __grid_constant__ CUtensorMap ts_shared, const GemvParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* stages = smem;
-  float* red = reinterpret_cast<float*>(smem + kGemvStages * kStageBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGemvStages * kStageBytes + kRedBytes);
-  uint64_t* empty = full + kGemvStages;
-  int* flag = reinterpret_cast<int*>(empty + kGemvStages);
-
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Dims& d = p.d;
   const bool scale_tma = p.scale_tma != 0;
   const int n_sh = shared_tasks<MODE>(d);
+  unsigned* err = p.r.err;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kGemvStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 8);
+    for (int i = 0; i < kGemvStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 8);
     }
+    mbar_init(&s.bar[kBarRedFull], 8);
+    mbar_init(&s.bar[kBarRedEmpty], 8);
+    mbar_init(&s.bar[kBarYDone], 8);
+    mbar_init(&s.bar[kBarFlag], 1);
     fence_mbar_init();
   }
   __syncthreads();
   pdl_launch_dependents();
 
   if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane != 0) return;
-    prefetch_tmap(&tm_routed);
-    prefetch_tmap(&tm_shared);
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_routed);
+      prefetch_tmap(&tm_shared);
+    }
     int stage = 0;
     uint32_t phase = 0;
-    bool waited = false;
-    // Stages whose weights went out before the dependency wait and whose
-    // activations (h of the previous kernel, for the down pass) are pending.
-    int pend_n = 0;
-    int pend_stage[kGemvStages], pend_g0[kGemvStages];
-    Task pend_task[kGemvStages];
-    int ntasks = -1;
-    for (int tau = blockIdx.x;; tau += gridDim.x) {
+    bool waited = false, stop = false;
+    int n_act = 0, n_routed = 0;
+    // stages whose activations (h of the previous kernel) wait for the dependency
+    int pn = 0;
+    int p_stage[kGemvStages], p_g0[kGemvStages];
+    Task p_task[kGemvStages];
+
+    auto resolve = [&]() {
+      pdl_wait();
+      waited = true;
+      n_act = p.r.meta[kMetaActive];
+      n_routed = p.r.meta[MODE == 1 ? kMetaTasks1 : kMetaTasks2];
+      const int* pre = (MODE == 1) ? p.r.task1 : p.r.task2;
+      for (int i = lane; i <= n_act; i += 32) {
+        s.prefix[i] = pre[i];
+        if (i < n_act) s.active[i] = p.r.active[i];
+      }
+      for (int i = lane; i <= d.E; i += 32) s.offsets[i] = p.r.offsets[i];
+      __syncwarp();
+      for (int i = 0; i < pn; ++i) {
+        const Task& t = p_task[i];
+        if (lane < t.nr)
+          bulk_copy(smem_u32(s.stage[p_stage[i]] + kXOff + lane * kXStride),
+                    act_row<MODE>(p, t, t.r0 + lane) + p_g0[i] * kGroup,
+                    min(8, t.ngroups - p_g0[i]) * 256, &s.full[p_stage[i]]);
+      }
+      pn = 0;
+    };
+
+    for (int tau = blockIdx.x; !stop; tau += gridDim.x) {
       const bool sh = tau < n_sh;
-      if (!sh && !waited) {
-        // flush pending activation copies after the dependency resolves
-        pdl_wait();
-        waited = true;
-        for (int i = 0; i < pend_n; ++i) {
-          const Task& pt = pend_task[i];
-          issue_acts<MODE>(p, stages + pend_stage[i] * kStageBytes, &full[pend_stage[i]], pt,
-                           pend_g0[i], min(8, pt.ngroups - pend_g0[i]));
-        }
-        pend_n = 0;
-      }
-      if (!sh) {
-        if (ntasks < 0) ntasks = n_sh + ((MODE == 1) ? p.r.meta[kMetaTasks1] : p.r.meta[kMetaTasks2]);
-        if (tau >= ntasks) break;
-      }
-      const Task t = sh ? shared_task<MODE>(d, tau) : routed_task<MODE>(p, tau - n_sh);
+      if (!sh && !waited) resolve();
+      if (!sh && tau >= n_sh + n_routed) break;
+      const Task t = sh ? make_task<MODE>(d, true, d.E, d.T * d.k, d.T * d.k + d.T, tau)
+                        : routed_task<MODE>(s, d, n_act, tau - n_sh);
       const CUtensorMap* tm = t.shared ? &tm_shared : &tm_routed;
       const CUtensorMap* ts = t.shared ? &ts_shared : &ts_routed;
-      bool stop = false;
+      const uint16_t* arow = nullptr;
+      if ((MODE == 1 || waited) && lane < t.nr) arow = act_row<MODE>(p, t, t.r0 + lane);
       for (int g0 = 0; g0 < t.ngroups; g0 += 8) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, p.r.err)) {
+        const int gcnt = min(8, t.ngroups - g0);
+        uint8_t* st = s.stage[stage];
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(&s.empty[stage], phase ^ 1u, err);
+          if (ok) {
+            Desc& ds = s.desc[stage];
+            ds.flags = (g0 == 0 ? kFirst : 0) | (g0 + 8 >= t.ngroups ? kLast : 0) |
+                       (t.shared ? kShared : 0);
+            ds.g0 = g0;
+            ds.gcnt = gcnt;
+            ds.ngroups = t.ngroups;
+            ds.tile = t.tile;
+            ds.r0 = t.r0;
+            ds.nr = t.nr;
+            ds.rowA0 = t.rowA0;
+            ds.rowA1 = t.rowA1;
+            mbar_arrive_expect_tx(&s.full[stage],
+                                  gcnt * 2 * 1024 + (scale_tma ? kSBytes : 0) + t.nr * gcnt * 256);
+            for (int g = 0; g < gcnt; ++g) {
+              tma_load_3d(st + g * 1024, tm, &s.full[stage], 0, g0 + g, t.rowA0);
+              tma_load_3d(st + (8 + g) * 1024, tm, &s.full[stage], 0, g0 + g, t.rowA1);
+            }
+            if (scale_tma) {
+              tma_load_2d(smem_u32(st + kWBytes), ts, &s.full[stage], g0, t.rowA0);
+              tma_load_2d(smem_u32(st + kWBytes + 256), ts, &s.full[stage], g0, t.rowA1);
+            }
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
           stop = true;
           break;
         }
-        const int gcnt = min(8, t.ngroups - g0);
-        uint8_t* st = stages + stage * kStageBytes;
-        mbar_arrive_expect_tx(&full[stage], stage_bytes<MODE>(t, gcnt, scale_tma));
-        issue_weights(st, &full[stage], tm, ts, t, g0, gcnt, scale_tma);
-        // gate/up reads x (an input): never waits. down reads h: its copies
-        // wait for the gate/up kernel; until then the stage is remembered.
         if (MODE == 1 || waited) {
-          issue_acts<MODE>(p, st, &full[stage], t, g0, gcnt);
-        } else if (pend_n < kGemvStages) {
-          pend_stage[pend_n] = stage;
-          pend_g0[pend_n] = g0;
-          pend_task[pend_n] = t;
-          ++pend_n;
+          if (lane < t.nr)
+            bulk_copy(smem_u32(st + kXOff + lane * kXStride), arow + g0 * kGroup, gcnt * 256,
+                      &s.full[stage]);
+        } else {
+          p_stage[pn] = stage;
+          p_g0[pn] = g0;
+          p_task[pn] = t;
+          ++pn;
         }
         if (++stage == kGemvStages) {
           stage = 0;
           phase ^= 1u;
         }
-        // the ring is full of pending stages: resolve the dependency now
-        if (MODE == 2 && !waited && pend_n == kGemvStages) {
-          pdl_wait();
-          waited = true;
-          for (int i = 0; i < pend_n; ++i) {
-            const Task& pt = pend_task[i];
-            issue_acts<MODE>(p, stages + pend_stage[i] * kStageBytes, &full[pend_stage[i]], pt,
-                             pend_g0[i], min(8, pt.ngroups - pend_g0[i]));
-          }
-          pend_n = 0;
-        }
+        if (MODE == 2 && !waited && pn == kGemvStages) resolve();
       }
-      if (stop) break;
     }
-    if (!waited) {
-      pdl_wait();
-      for (int i = 0; i < pend_n; ++i) {
-        const Task& pt = pend_task[i];
-        issue_acts<MODE>(p, stages + pend_stage[i] * kStageBytes, &full[pend_stage[i]], pt,
-                         pend_g0[i], min(8, pt.ngroups - pend_g0[i]));
-      }
+    if (!waited) resolve();
+    // end-of-work marker for the consumers
+    if (lane == 0 && !stop && mbar_wait(&s.empty[stage], phase ^ 1u, err)) {
+      s.desc[stage].flags = kEnd;
+      mbar_arrive(&s.full[stage]);
     }
     return;
   }
 
-  // -------------------------------------------------------------- consumers
+  // ---------------------------------------------------------------- consumers
   const int g = lane >> 2, c = lane & 3;
+  const uint32_t stage0 = smem_u32(s.stage[0]);
+  const uint32_t w_off = warp * 1024 + g * 64 + c * 16;
+  const uint32_t s_off = kWBytes + g * 16 + warp * 2;
+  const uint32_t x_off = kXOff + g * kXStride + warp * 256 + c * 64;
   int stage = 0;
-  uint32_t phase = 0;
-  bool ok = true;
+  uint32_t phase = 0, tphase = 0;
   bool waited = false;
-  int ntasks = -1;
-  for (int tau = blockIdx.x;; tau += gridDim.x) {
-    const bool sh = tau < n_sh;
-    if (!sh) {
-      if (!waited) {
-        pdl_wait();
-        waited = true;
-      }
-      if (ntasks < 0) ntasks = n_sh + ((MODE == 1) ? p.r.meta[kMetaTasks1] : p.r.meta[kMetaTasks2]);
-      if (tau >= ntasks) break;
+  float acc[2][4] = {};
+  for (;;) {
+    if (!mbar_wait(&s.full[stage], phase, err)) break;
+    const Desc ds = s.desc[stage];
+    if (ds.flags & kEnd) break;
+    if (ds.flags & kFirst) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[0][i] = acc[1][i] = 0.f;
     }
-    const Task t = sh ? shared_task<MODE>(d, tau) : routed_task<MODE>(p, tau - n_sh);
-    const int ng = t.ngroups;
-    const uint16_t* scales = t.shared ? p.scale_shared : p.scale_routed;
-    const size_t s00 = (size_t)(t.rowA0 + g) * ng, s01 = s00 + (size_t)8 * ng;
-    const size_t s10 = (size_t)(t.rowA1 + g) * ng, s11 = s10 + (size_t)8 * ng;
-    const bool has_row = g < t.nr;
-    float acc[2][4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) acc[i][q] = 0.f;
-
-    for (int g0 = 0; g0 < ng; g0 += 8) {
-      const int gi = g0 + warp;
-      const bool mine = gi < ng;
+    if (warp < ds.gcnt) {
+      const int gi = ds.g0 + warp;
+      const uint32_t st = stage0 + stage * kStageBytes;
+      const uint4 w00 = lds128(st + w_off), w01 = lds128(st + w_off + 8 * 64);
+      const uint4 w10 = lds128(st + w_off + 8 * 1024), w11 = lds128(st + w_off + 8 * 1024 + 8 * 64);
       float sc[4];
-      if (mine && !scale_tma) {
-        sc[0] = bf16_bits_to_f32(__ldg(scales + s00 + gi));
-        sc[1] = bf16_bits_to_f32(__ldg(scales + s01 + gi));
-        sc[2] = bf16_bits_to_f32(__ldg(scales + s10 + gi));
-        sc[3] = bf16_bits_to_f32(__ldg(scales + s11 + gi));
+      if (scale_tma) {
+        sc[0] = bf16_bits_to_f32(lds16(st + s_off));
+        sc[1] = bf16_bits_to_f32(lds16(st + s_off + 8 * 16));
+        sc[2] = bf16_bits_to_f32(lds16(st + s_off + 256));
+        sc[3] = bf16_bits_to_f32(lds16(st + s_off + 256 + 8 * 16));
+      } else {
+        const uint16_t* scl = (ds.flags & kShared) ? p.scale_shared : p.scale_routed;
+        const int ng = ds.ngroups;
+        sc[0] = bf16_bits_to_f32(__ldg(scl + (size_t)(ds.rowA0 + g) * ng + gi));
+        sc[1] = bf16_bits_to_f32(__ldg(scl + (size_t)(ds.rowA0 + g + 8) * ng + gi));
+        sc[2] = bf16_bits_to_f32(__ldg(scl + (size_t)(ds.rowA1 + g) * ng + gi));
+        sc[3] = bf16_bits_to_f32(__ldg(scl + (size_t)(ds.rowA1 + g + 8) * ng + gi));
       }
-      if (ok) ok = mbar_wait(&full[stage], phase, p.r.err);
-      if (mine && ok) {
-        const uint32_t st = smem_u32(stages + stage * kStageBytes);
-        const uint32_t wa = st + warp * 1024 + g * 64 + c * 16;
-        const uint4 w00 = lds128(wa), w01 = lds128(wa + 8 * 64);
-        const uint4 w10 = lds128(wa + 8 * 1024), w11 = lds128(wa + 8 * 1024 + 8 * 64);
-        if (scale_tma) {
-          const uint32_t sa = st + kWBytes + g * 16 + warp * 2;
-          sc[0] = bf16_bits_to_f32(lds16(sa));
-          sc[1] = bf16_bits_to_f32(lds16(sa + 8 * 16));
-          sc[2] = bf16_bits_to_f32(lds16(sa + 256));
-          sc[3] = bf16_bits_to_f32(lds16(sa + 256 + 8 * 16));
-        }
-        uint4 b[4];
-        if (has_row) {
-          const uint32_t xa = st + kXOff + g * kXStride + warp * 256 + c * 64;
+      uint4 b[4];
+      if (g < ds.nr) {
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            b[m] = lds128(xa + m * 16);
-            if (MODE == 1) b[m] = interleave8(b[m]);
-          }
-        } else {
-#pragma unroll
-          for (int m = 0; m < 4; ++m) b[m] = make_uint4(0u, 0u, 0u, 0u);
+        for (int m = 0; m < 4; ++m) {
+          b[m] = lds128(st + x_off + m * 16);
+          if (MODE == 1) b[m] = interleave8(b[m]);
         }
-        float tmp[4];
-        group_mma(w00, w01, b, tmp);
-        acc[0][0] = fmaf(sc[0], tmp[0], acc[0][0]);
-        acc[0][1] = fmaf(sc[0], tmp[1], acc[0][1]);
-        acc[0][2] = fmaf(sc[1], tmp[2], acc[0][2]);
-        acc[0][3] = fmaf(sc[1], tmp[3], acc[0][3]);
-        group_mma(w10, w11, b, tmp);
-        acc[1][0] = fmaf(sc[2], tmp[0], acc[1][0]);
-        acc[1][1] = fmaf(sc[2], tmp[1], acc[1][1]);
-        acc[1][2] = fmaf(sc[3], tmp[2], acc[1][2]);
-        acc[1][3] = fmaf(sc[3], tmp[3], acc[1][3]);
+      } else {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) b[m] = make_uint4(0u, 0u, 0u, 0u);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-      if (++stage == kGemvStages) {
-        stage = 0;
-        phase ^= 1u;
-      }
+      float tmp[4];
+      group_mma(w00, w01, b, tmp);
+      acc[0][0] = fmaf(sc[0], tmp[0], acc[0][0]);
+      acc[0][1] = fmaf(sc[0], tmp[1], acc[0][1]);
+      acc[0][2] = fmaf(sc[1], tmp[2], acc[0][2]);
+      acc[0][3] = fmaf(sc[1], tmp[3], acc[0][3]);
+      group_mma(w10, w11, b, tmp);
+      acc[1][0] = fmaf(sc[2], tmp[0], acc[1][0]);
+      acc[1][1] = fmaf(sc[2], tmp[1], acc[1][1]);
+      acc[1][2] = fmaf(sc[3], tmp[2], acc[1][2]);
+      acc[1][3] = fmaf(sc[3], tmp[3], acc[1][3]);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.empty[stage]);
+    if (++stage == kGemvStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    if (!(ds.flags & kLast)) continue;
 
-    // ---- deterministic cross-warp reduction and epilogue
-    float4* redw = reinterpret_cast<float4*>(red);
-    redw[(warp * 2 + 0) * 32 + lane] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
-    redw[(warp * 2 + 1) * 32 + lane] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
-    named_bar_consumers();
+    // ---- end of a task: deterministic cross-warp reduction and epilogue
+    if (!mbar_wait(&s.bar[kBarRedEmpty], tphase ^ 1u, err)) break;
+    s.red[(warp * 2 + 0) * 32 + lane] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+    s.red[(warp * 2 + 1) * 32 + lane] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.bar[kBarRedFull]);
+    if (!mbar_wait(&s.bar[kBarRedFull], tphase, err)) break;
+    const float* red = reinterpret_cast<const float*>(s.red);
     if (MODE == 1) {
       if (threadIdx.x < 16 * kRows) {
         const int row = threadIdx.x >> 3, tok = threadIdx.x & 7;
@@ -449,10 +440,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
           v0 += red[((w * 2 + 0) * 32 + ln) * 4 + q];
           v1 += red[((w * 2 + 1) * 32 + ln) * 4 + q];
         }
-        if (tok < t.nr) {
-          const int n = t.tile * kTile1 + row;
+        if (tok < ds.nr) {
+          const int n = ds.tile * kTile1 + row;
           const int pos = (n & ~7) | ((n & 3) << 1) | ((n >> 2) & 1);
-          p.hout[(size_t)(t.r0 + tok) * p.hstride + pos] = f32_to_bf16_bits(silu(v0) * v1);
+          p.hout[(size_t)(ds.r0 + tok) * p.hstride + pos] = f32_to_bf16_bits(silu(v0) * v1);
         }
       }
     } else {
@@ -461,24 +452,32 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       float v = 0.f;
 #pragma unroll
       for (int w = 0; w < 8; ++w) v += red[((w * 2 + tl) * 32 + ln) * 4 + q];
-      if (tok < t.nr) p.yout[(size_t)(t.r0 + tok) * d.H + t.tile * kTile2 + tl * 16 + row] = v;
+      if (tok < ds.nr) p.yout[(size_t)(ds.r0 + tok) * d.H + ds.tile * kTile2 + tl * 16 + row] = v;
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.bar[kBarRedEmpty]);
+
     if (MODE == 2 && p.fuse_combine) {
-      // last task to finish this channel tile combines it for every token
+      // the last task to finish this channel tile combines it for every token
       if (!waited) {  // routing results are read below
         pdl_wait();
         waited = true;
       }
-      __threadfence();
-      named_bar_consumers();
+      if (lane == 0) mbar_arrive(&s.bar[kBarYDone]);
       if (threadIdx.x == 0) {
-        const int per_tile = (n_sh + p.r.meta[kMetaTasks2]) / (d.H / kTile2);
-        *flag = (atomicAdd(&p.tile_cnt[t.tile], 1) == per_tile - 1);
+        if (mbar_wait(&s.bar[kBarYDone], tphase, err)) {
+          __threadfence();
+          const int per_tile = (n_sh + p.r.meta[kMetaTasks2]) / (d.H / kTile2);
+          s.flag = (atomicAdd(&p.tile_cnt[ds.tile], 1) == per_tile - 1);
+        } else {
+          s.flag = 0;
+        }
+        mbar_arrive(&s.bar[kBarFlag]);
       }
-      named_bar_consumers();
-      if (*flag) {
+      if (!mbar_wait(&s.bar[kBarFlag], tphase, err)) break;
+      if (s.flag) {
         __threadfence();
-        const int n0 = t.tile * kTile2;
+        const int n0 = ds.tile * kTile2;
         for (int i = threadIdx.x; i < d.T * kTile2; i += 256) {
           const int tok = i / kTile2, n = n0 + (i - tok * kTile2);
           float a = d.Is > 0 ? __ldcg(p.yout + (size_t)(d.T * d.k + tok) * d.H + n) : 0.f;
@@ -489,10 +488,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
           }
           p.out[(size_t)tok * d.H + n] = f32_to_bf16_bits(a);
         }
-        if (threadIdx.x == 0) p.tile_cnt[t.tile] = 0;
+        if (threadIdx.x == 0) p.tile_cnt[ds.tile] = 0;
       }
     }
-    named_bar_consumers();
+    tphase ^= 1u;
   }
 }
 

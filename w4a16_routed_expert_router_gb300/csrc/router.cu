@@ -91,59 +91,76 @@ __device__ __forceinline__ void warp_topk(const float* logit_row, const float* b
   *out_w = chosen_s / sum;
 }
 
-// Exclusive scan of one value per thread across a 256-thread block.
-__device__ __forceinline__ int block_scan_256(int v, int* scratch /* >= 8 ints */, int* total) {
+// Exclusive scan of four values per thread across a 256-thread block;
+// scratch >= 8 int4. Returns the exclusive prefix, *total the block sums.
+__device__ __forceinline__ int4 block_scan4_256(int4 v, int4* scratch, int4* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int inc = v;
+  int4 inc = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += n;
+    const int a = __shfl_up_sync(0xffffffffu, inc.x, o), b = __shfl_up_sync(0xffffffffu, inc.y, o);
+    const int c = __shfl_up_sync(0xffffffffu, inc.z, o), e = __shfl_up_sync(0xffffffffu, inc.w, o);
+    if (lane >= o) {
+      inc.x += a;
+      inc.y += b;
+      inc.z += c;
+      inc.w += e;
+    }
   }
   if (lane == 31) scratch[warp] = inc;
   __syncthreads();
-  int base = 0, tot = 0;
+  int4 base = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
-    const int s = scratch[w];
-    if (w < warp) base += s;
-    tot += s;
+    const int4 s = scratch[w];
+    if (w < warp) {
+      base.x += s.x;
+      base.y += s.y;
+      base.z += s.z;
+      base.w += s.w;
+    }
+    tot.x += s.x;
+    tot.y += s.y;
+    tot.z += s.z;
+    tot.w += s.w;
   }
-  __syncthreads();
   *total = tot;
-  return base + inc - v;
+  return make_int4(base.x + inc.x - v.x, base.y + inc.y - v.y, base.z + inc.z - v.z,
+                   base.w + inc.w - v.w);
 }
 
-// Active routed experts (ascending) and the prefix of their expert-kernel
-// tasks, run by one 256-thread block once counts_s (shared [E]) is final.
-// The shared expert's tasks are not listed: the expert kernels put them first.
-__device__ void build_task_lists(const Dims& d, const int* counts_s, const Routing& r,
-                                 int* scratch) {
+// From final per-expert row counts (shared, [E]): offsets (exclusive scan,
+// also left in offs_s), counts, the ascending list of active routed experts
+// and the prefix of their expert-kernel tasks, and the meta words. One
+// 256-thread block. The shared expert's tasks are not listed: the expert
+// kernels put them first.
+__device__ void finish_counts(const Dims& d, const int* counts_s, int* offs_s, const Routing& r,
+                              int4* scratch) {
   const int e = threadIdx.x;
   const int c = (e < d.E) ? counts_s[e] : 0;
-  int n_act;
-  const int idx = block_scan_256(c > 0 ? 1 : 0, scratch, &n_act);
-  int c1 = 0, c2 = 0;
-  if (e < d.E && c > 0) {
-    const int p = passes_for(c);
-    c1 = p * (d.I / kTile1);
-    c2 = p * (d.H / kTile2);
-  }
-  int s1, s2;
-  const int x1 = block_scan_256(c1, scratch, &s1);
-  const int x2 = block_scan_256(c2, scratch, &s2);
-  if (e < d.E && c > 0) {
-    r.active[idx] = e;
-    r.task1[idx] = x1;
-    r.task2[idx] = x2;
+  const int p = passes_for(c);
+  const int4 v = make_int4(c, c > 0 ? 1 : 0, p * (d.I / kTile1), p * (d.H / kTile2));
+  int4 tot;
+  const int4 ex = block_scan4_256(v, scratch, &tot);
+  if (e < d.E) {
+    offs_s[e] = ex.x;
+    r.offsets[e] = ex.x;
+    r.counts[e] = c;
+    if (c > 0) {
+      r.active[ex.y] = e;
+      r.task1[ex.y] = ex.z;
+      r.task2[ex.y] = ex.w;
+    }
   }
   if (threadIdx.x == 0) {
-    r.task1[n_act] = s1;
-    r.task2[n_act] = s2;
-    r.meta[kMetaActive] = n_act;
-    r.meta[kMetaTasks1] = s1;
-    r.meta[kMetaTasks2] = s2;
+    r.offsets[d.E] = tot.x;
+    r.task1[tot.y] = tot.z;
+    r.task2[tot.y] = tot.w;
+    r.meta[kMetaActive] = tot.y;
+    r.meta[kMetaTasks1] = tot.z;
+    r.meta[kMetaTasks2] = tot.w;
   }
+  __syncthreads();
 }
 
 }  // namespace
@@ -151,7 +168,7 @@ __device__ void build_task_lists(const Dims& d, const int* counts_s, const Routi
 // ----------------------------------------------------------------- small T
 // grid: ceil(E / 2) CTAs x 256 threads. Warps 0-3 score expert 2b, warps 4-7
 // expert 2b+1, each warp a quarter of H. Requires T <= kSmallT, H % 512 == 0.
-__global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(256, 1) route_small_kernel(const uint16_t* __restrict__ x,
                                                           const float* __restrict__ router_w,
                                                           const float* __restrict__ bias, Dims d,
                                                           Routing r) {
@@ -159,7 +176,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
   __shared__ int ids_s[kSmallT * kMaxTopK];
   __shared__ int counts_s[kMaxExperts];
   __shared__ int offs_s[kMaxExperts];
-  __shared__ int scratch[16];
+  __shared__ int4 scratch[8];
   __shared__ float lbuf[8][kMaxExperts];
   __shared__ unsigned last;
 
@@ -215,33 +232,28 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
     }
   }
 
-  // ---- last CTA finishes routing for all tokens
-  __threadfence();
+  // ---- the last CTA to finish finishes the routing of all tokens
   __syncthreads();
-  if (threadIdx.x == 0) last = (atomicAdd(&r.tickets[kTicketRouter], 1u) == gridDim.x - 1);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = (atomicAdd(&r.tickets[kTicketRouter], 1u) == gridDim.x - 1);
+  }
   __syncthreads();
   if (!last) return;
   __threadfence();
 
-  for (int i = threadIdx.x; i < d.E; i += blockDim.x) counts_s[i] = 0;
+  if (threadIdx.x < kMaxExperts) counts_s[threadIdx.x] = 0;
   __syncthreads();
   for (int t = warp; t < d.T; t += 8) {
     const float* lrow = r.logits + (size_t)t * d.E;
-    int id;
-    float w;
-    // logits were written by other CTAs: read through L2
-    float lv[kMaxExperts / 32];
 #pragma unroll
     for (int i = 0; i < kMaxExperts / 32; ++i) {
       const int ee = lane + 32 * i;
-      lv[i] = (ee < d.E) ? __ldcg(lrow + ee) : 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
-      const int ee = lane + 32 * i;
-      if (ee < d.E) lbuf[warp][ee] = lv[i];
+      if (ee < d.E) lbuf[warp][ee] = __ldcg(lrow + ee);
     }
     __syncwarp();
+    int id;
+    float w;
     warp_topk(lbuf[warp], bias, d.E, d.k, lane, &id, &w);
     __syncwarp();
     if (lane < d.k) {
@@ -256,19 +268,8 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
     }
   }
   __syncthreads();
-  int total;
-  {
-    const int c = (threadIdx.x < d.E) ? counts_s[threadIdx.x] : 0;
-    const int ex = block_scan_256(c, scratch, &total);
-    if (threadIdx.x < d.E) {
-      offs_s[threadIdx.x] = ex;
-      r.offsets[threadIdx.x] = ex;
-      r.counts[threadIdx.x] = c;
-    }
-    if (threadIdx.x == 0) r.offsets[d.E] = total;
-  }
-  __syncthreads();
-  // stable placement: rank of item i among earlier items with the same expert
+  finish_counts(d, counts_s, offs_s, r, scratch);
+  // stable placement: rank of item i among earlier items of the same expert
   const int n = d.T * d.k;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const int ei = ids_s[i];
@@ -278,7 +279,6 @@ __global__ void __launch_bounds__(256) route_small_kernel(const uint16_t* __rest
     r.perm[pos] = i / d.k;
     r.inv[i] = pos;
   }
-  build_task_lists(d, counts_s, r, scratch);
   if (threadIdx.x == 0) r.tickets[kTicketRouter] = 0u;
 }
 
@@ -337,7 +337,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
                                                           Routing r) {
   __shared__ int hist[kMaxExperts];
   __shared__ int counts_s[kMaxExperts];
-  __shared__ int scratch[16];
+  __shared__ int offs_s[kMaxExperts];
+  __shared__ int4 scratch[8];
   __shared__ unsigned last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kMaxExperts; i += blockDim.x) hist[i] = 0;
@@ -360,9 +361,11 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
   __syncthreads();
   for (int i = threadIdx.x; i < d.E; i += blockDim.x)
     r.blockcnt[(size_t)blockIdx.x * d.E + i] = hist[i];
-  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) last = (atomicAdd(&r.tickets[kTicketTopk], 1u) == gridDim.x - 1);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = (atomicAdd(&r.tickets[kTicketTopk], 1u) == gridDim.x - 1);
+  }
   __syncthreads();
   if (!last) return;
   __threadfence();
@@ -371,21 +374,16 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
   int c = 0;
   if (e < d.E)
     for (int b = 0; b < nblk; ++b) c += __ldcg(r.blockcnt + (size_t)b * d.E + e);
-  int total;
-  const int ex = block_scan_256(c, scratch, &total);
+  if (e < kMaxExperts) counts_s[e] = c;
+  __syncthreads();
+  finish_counts(d, counts_s, offs_s, r, scratch);
   if (e < d.E) {
-    counts_s[e] = c;
-    r.counts[e] = c;
-    r.offsets[e] = ex;
-    int run = ex;
+    int run = offs_s[e];
     for (int b = 0; b < nblk; ++b) {
       r.blockbase[(size_t)b * d.E + e] = run;
       run += __ldcg(r.blockcnt + (size_t)b * d.E + e);
     }
   }
-  if (threadIdx.x == 0) r.offsets[d.E] = total;
-  __syncthreads();
-  build_task_lists(d, counts_s, r, scratch);
   if (threadIdx.x == 0) r.tickets[kTicketTopk] = 0u;
 }
 
