@@ -153,7 +153,7 @@ def _full_case(full, name, sample):
 
 def test_decode1_full_layer(full):
     rt, names = _full_case(full, "decode1", lambda r, T: np.arange(T))
-    assert names == ["route_small", "gemv_gate_up_swiglu", "gemv_down_combine"]
+    assert names == ["decode_fused"]
 
 
 def test_decode64_routing_and_sampled_outputs(full):

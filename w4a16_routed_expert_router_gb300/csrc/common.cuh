@@ -131,13 +131,11 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
 // Two 4-bit codes -> two exact bf16 integers q = u - 8.
 // Codes j and j+4 of a word (bits 4j.. and 4j+16..) are moved into the low
 // mantissa bits of two bf16 values of exponent 2^7, giving 128 + u exactly
-// (the bf16 spacing at 128 is 1); subtracting 136 leaves u - 8. The right
-// shift by 4j is a high-half multiply by 2^(32-4j), which runs on the FMA
-// pipe and leaves the integer ALU pipe to the lop3.
+// (the bf16 spacing at 128 is 1); subtracting 136 leaves u - 8.
 template <int J>
 __device__ __forceinline__ uint32_t int4_pair_to_bf16x2(uint32_t word) {
   uint32_t v;
-  const uint32_t w = (J == 0) ? word : __umulhi(word, 1u << (32 - 4 * J));
+  const uint32_t w = word >> (4 * J);
   asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(v) : "r"(w), "r"(0x000F000Fu), "r"(0x43004300u));
   __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&v);
   const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);

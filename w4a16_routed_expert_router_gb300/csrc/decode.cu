@@ -1,0 +1,888 @@
+// Decode-sized forward (T <= kSmallT tokens) as ONE persistent cooperative
+// kernel: router, gate/up + SwiGLU, down, weighted combine with the shared
+// expert.
+//
+// At decode sizes the layer is a stream of INT4 weights: about 91 MB of
+// expert weights plus the 4 MB fp32 router at one token ("Throughputmaxxing:
+// DeepSeek-V4-Flash on Isambard-AI", "A pass through the model": below the
+// ridge the expert GEMMs are memory bound; "Where does the time go?": the
+// act+quant bucket is hundreds of tiny launches). Each kernel boundary costs a
+// ramp-up and a tail of the memory pipeline, so the whole layer runs as one
+// task stream that never stops fetching weights:
+//
+//   [gate/up shared | down shared | gate/up routed | down routed]
+//
+// CTA b takes tasks b, b + G, b + 2G, ... (G = one CTA per SM). A task covers
+// two 16-row weight tiles (16 gate + 16 up channels, or 32 down channels) of
+// one expert over all of K, for one pass of <= 8 rows of that expert.
+//
+//  * Router: consumer warps of every CTA first score one or two experts for
+//    all tokens (fp32). The CTA that finishes last (atomic ticket) runs top-k,
+//    histogram, scan, the stable permutation and the task lists, then
+//    publishes a ready flag. The shared expert's tasks need no routing and
+//    keep the memory system busy meanwhile.
+//  * Producer warp: decodes tasks, fills a 6-stage ring (2-D TMA boxes of 16
+//    rows x 512 B per tile, scale boxes, bulk copies of the activation rows)
+//    and hands each stage a descriptor. Down tasks need the h rows of their
+//    (expert, pass): their weights are prefetched at once, their h copies wait
+//    on a per-(expert, pass) completion counter.
+//  * 16 consumer warps: warp w takes K-group (w % 8) of tile (w / 8) of every
+//    stage; exact INT4 -> bf16 in registers, mma.sync m16n8k16 with weights as
+//    A and up to 8 rows as B, group scales applied in fp32.
+//  * Gate/up epilogue: SwiGLU -> bf16 h, then +1 on the (expert, pass)
+//    counter. Down epilogue: fp32 y; the last task of a channel tile combines
+//    the tile for every token (out = y_shared + sum_j w_j y_j, slot order).
+//  * Every wait is bounded in time and gives up once any wait of the grid has
+//    timed out (device error flag), so a broken hand-off cannot hang the GPU.
+//    The grid is launched cooperatively so all CTAs are co-resident; every
+//    CTA finishes all its gate/up tasks before any down task, so waits on
+//    counters always make progress. The last CTA to exit resets the counters.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kCW = 16;                      // consumer warps
+constexpr int kThreads = (kCW + 1) * 32;     // + one producer warp
+constexpr int kR = 8;                        // rows per pass (MMA N)
+constexpr int kS = 6;                        // ring stages
+constexpr int kWB = 2 * 16 * 512;            // 2 tiles x 16 rows x 512 B (8 K-groups)
+constexpr int kSB = 2 * 16 * 16;             // 2 tiles x 16 rows x 8 bf16 scales
+constexpr int kXS = 8 * 256 + 64;            // one activation row (8 groups bf16) + pad
+constexpr int kXO = kWB + kSB;
+constexpr int kStageB = (kXO + kR * kXS + 1023) / 1024 * 1024;
+constexpr int kMaxPass = (kSmallT + kR - 1) / kR;  // passes per expert at most
+
+enum { kFirst = 1, kLast = 2, kEnd = 4, kShared = 8, kDown = 16 };
+
+struct Desc {
+  int flags, g0, gcnt, ngroups, tile, r0, nr, rowA0, rowA1, cnt, pad[2];
+};
+
+enum { kBarRedFull = 0, kBarRedEmpty, kBarDone, kBarFlag, kNumBars };
+
+struct Smem {
+  uint8_t stage[kS][kStageB];
+  union {
+    float4 red[kCW * 32];               // task-end partial sums
+    float part[2][kCW][kSmallT];        // router: per-warp partial logits of 2 experts
+    float lbuf[kCW][kMaxExperts];       // router finish: one token's logits per warp
+  } u;
+  int ids_s[kSmallT * kMaxTopK];
+  int counts_s[kMaxExperts];
+  int offs_s[kMaxExperts];
+  int4 scan[kCW];
+  Desc desc[kS];
+  int active[kMaxExperts + 2];
+  int pre1[kMaxExperts + 2];
+  int pre2[kMaxExperts + 2];
+  int offsets[kMaxExperts + 2];
+  int meta[4];                          // n_act, routed gate/up tasks, routed down tasks
+  uint64_t full[kS];
+  uint64_t empty[kS];
+  uint64_t bar[kNumBars];
+  int flag;
+};
+
+struct DecodeParams {
+  Dims d;
+  Routing r;
+  const uint16_t* x;            // [T, H] bf16
+  const float* router_w;        // [E, H]
+  const float* router_bias;     // [E]
+  const uint16_t* s13_routed;   // scales, for the consumers when not TMA'd
+  const uint16_t* s13_shared;
+  const uint16_t* s2_routed;
+  const uint16_t* s2_shared;
+  uint16_t* h;                  // [rows, hstride] bf16, interleaved
+  int hstride;
+  float* y;                     // [rows, H] fp32
+  uint16_t* out;                // [T, H] bf16
+  int* done1;                   // [(E + 1) * kMaxPass] gate/up tasks done per (expert, pass)
+  int* tile_cnt;                // [H / 32] down tasks done per channel tile
+  unsigned* sync;               // [4]: router ticket, ready flag, exit ticket
+  int scale_tma;
+};
+
+struct Task {
+  bool down, shared;
+  int e, ngroups, rowA0, rowA1, r0, nr, tile, pass, cnt_target;
+};
+
+__device__ __forceinline__ int passes_of(int rows) { return (rows + kR - 1) / kR; }
+
+__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+
+__device__ __forceinline__ bool aborted(const unsigned* err) {
+  return (*reinterpret_cast<const volatile unsigned*>(err) & kErrTimeout) != 0;
+}
+
+// mbarrier wait bounded in time that also gives up once the grid aborted.
+__device__ __forceinline__ bool dwait(uint64_t* bar, uint32_t parity, unsigned* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (aborted(err)) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait until *p >= target (acquire). false on timeout / abort.
+__device__ __forceinline__ bool wait_counter(const int* p, int target, unsigned* err) {
+  if (ld_acquire(p) >= target) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (ld_acquire(p) >= target) return true;
+    if (aborted(err)) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint16_t lds16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
+                                       int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
+  return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
+}
+
+// ------------------------------------------------------------ task decode
+struct Counts {
+  int sh1, r1, sh2, r2, n_act;
+};
+
+__device__ __forceinline__ Task make_task(const Dims& d, bool down, bool shared, int e, int seg0,
+                                          int seg1, int local) {
+  Task t;
+  t.down = down;
+  t.shared = shared;
+  t.e = e;
+  const int passes = passes_of(seg1 - seg0);
+  t.tile = local / passes;
+  t.pass = local - t.tile * passes;
+  t.r0 = seg0 + t.pass * kR;
+  t.nr = min(kR, seg1 - t.r0);
+  const int inter = shared ? d.Is : d.I;
+  if (!down) {
+    t.ngroups = d.H / kGroup;
+    t.rowA0 = (shared ? 0 : e * 2 * inter) + t.tile * kTile1;
+    t.rowA1 = t.rowA0 + inter;
+    t.cnt_target = 0;
+  } else {
+    t.ngroups = inter / kGroup;
+    t.rowA0 = (shared ? 0 : e * d.H) + t.tile * kTile2;
+    t.rowA1 = t.rowA0 + 16;
+    t.cnt_target = inter / kTile1;  // gate/up tiles of this (expert, pass)
+  }
+  return t;
+}
+
+__device__ __forceinline__ int find_active(const int* pre, int n_act, int tau) {
+  int lo = 0, hi = n_act - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= tau)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// Task tau of the concatenated list [gate/up shared | down shared | gate/up
+// routed | down routed], or t.ngroups == 0 when tau is past its end.
+__device__ __forceinline__ Task task_at(const Smem& s, const Dims& d, const Counts& c, int tau) {
+  const int sh0 = d.T * d.k, sh1 = d.T * d.k + d.T;
+  if (tau < c.sh1) return make_task(d, false, true, d.E, sh0, sh1, tau);
+  tau -= c.sh1;
+  if (tau < c.sh2) return make_task(d, true, true, d.E, sh0, sh1, tau);
+  tau -= c.sh2;
+  if (tau < c.r1) {
+    const int a = find_active(s.pre1, c.n_act, tau);
+    const int e = s.active[a];
+    return make_task(d, false, false, e, s.offsets[e], s.offsets[e + 1], tau - s.pre1[a]);
+  }
+  tau -= c.r1;
+  if (tau < c.r2) {
+    const int a = find_active(s.pre2, c.n_act, tau);
+    const int e = s.active[a];
+    return make_task(d, true, false, e, s.offsets[e], s.offsets[e + 1], tau - s.pre2[a]);
+  }
+  Task t{};
+  t.ngroups = 0;
+  return t;
+}
+
+// ------------------------------------------------------------ router (consumers)
+__device__ __forceinline__ void warp_topk(const float* logit_row, const float* bias, int E, int k,
+                                          int lane, int* out_id, float* out_w) {
+  constexpr int kPer = kMaxExperts / 32;
+  float sel[kPer], sc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float s = 1.0f / (1.0f + expf(-logit_row[e]));
+      sc[i] = s;
+      sel[i] = s + bias[e];
+    } else {
+      sc[i] = 0.f;
+      sel[i] = -INFINITY;
+    }
+  }
+  float chosen_s = 0.f;
+  int chosen_e = -1;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      if (sel[i] > bv || (sel[i] == bv && e < be)) {
+        bv = sel[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    float ws = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (lane + 32 * i == be) {
+        ws = sc[i];
+        sel[i] = -INFINITY;
+      }
+    ws = __shfl_sync(0xffffffffu, ws, be & 31);
+    if (lane == j) {
+      chosen_e = be;
+      chosen_s = ws;
+    }
+  }
+  float sum = 0.f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, chosen_s, j);
+  *out_id = chosen_e;
+  *out_w = chosen_s / sum;
+}
+
+// Exclusive scan of four ints over the 512 consumer threads.
+__device__ __forceinline__ int4 cscan4(int4 v, int4* scr, int4* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int4 inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, inc.x, o), b = __shfl_up_sync(0xffffffffu, inc.y, o);
+    const int c = __shfl_up_sync(0xffffffffu, inc.z, o), e = __shfl_up_sync(0xffffffffu, inc.w, o);
+    if (lane >= o) {
+      inc.x += a;
+      inc.y += b;
+      inc.z += c;
+      inc.w += e;
+    }
+  }
+  if (lane == 31) scr[warp] = inc;
+  cbar();
+  int4 base = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
+  for (int w = 0; w < kCW; ++w) {
+    const int4 s = scr[w];
+    if (w < warp) {
+      base.x += s.x;
+      base.y += s.y;
+      base.z += s.z;
+      base.w += s.w;
+    }
+    tot.x += s.x;
+    tot.y += s.y;
+    tot.z += s.z;
+    tot.w += s.w;
+  }
+  cbar();
+  *total = tot;
+  return make_int4(base.x + inc.x - v.x, base.y + inc.y - v.y, base.z + inc.z - v.z,
+                   base.w + inc.w - v.w);
+}
+
+// Consumer warps: score this CTA's experts; the last CTA finishes the routing.
+__device__ void router_phase(Smem& s, const DecodeParams& p) {
+  const Dims& d = p.d;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int kw = d.H / kCW;  // K slice of one warp
+  const int nf = kw / 4;
+  for (int eb = blockIdx.x; eb < d.E; eb += 2 * gridDim.x) {
+    const int e0 = eb, e1 = eb + gridDim.x;
+    const bool has1 = e1 < d.E;
+    const float4* w0 = reinterpret_cast<const float4*>(p.router_w + (size_t)e0 * d.H + warp * kw);
+    const float4* w1 = reinterpret_cast<const float4*>(p.router_w + (size_t)(has1 ? e1 : e0) * d.H +
+                                                       warp * kw);
+    for (int t = 0; t < d.T; ++t) {
+      const uint2* xr = reinterpret_cast<const uint2*>(p.x + (size_t)t * d.H + warp * kw);
+      float a0 = 0.f, a1 = 0.f;
+      for (int f0 = 0; f0 < nf; f0 += 64) {
+        float4 v0[2], v1[2];
+        uint2 xv[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int f = f0 + u * 32 + lane;
+          const bool ok = f < nf;
+          v0[u] = ok ? __ldg(w0 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v1[u] = ok && has1 ? __ldg(w1 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+          xv[u] = ok ? __ldg(xr + f) : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float x0 = __uint_as_float(xv[u].x << 16), x1 = __uint_as_float(xv[u].x & 0xffff0000u);
+          const float x2 = __uint_as_float(xv[u].y << 16), x3 = __uint_as_float(xv[u].y & 0xffff0000u);
+          a0 = fmaf(x0, v0[u].x, a0);
+          a0 = fmaf(x1, v0[u].y, a0);
+          a0 = fmaf(x2, v0[u].z, a0);
+          a0 = fmaf(x3, v0[u].w, a0);
+          a1 = fmaf(x0, v1[u].x, a1);
+          a1 = fmaf(x1, v1[u].y, a1);
+          a1 = fmaf(x2, v1[u].z, a1);
+          a1 = fmaf(x3, v1[u].w, a1);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+        a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+      }
+      if (lane == 0) {
+        s.u.part[0][warp][t] = a0;
+        s.u.part[1][warp][t] = a1;
+      }
+    }
+    cbar();
+    if (tid < 2 * d.T) {
+      const int slot = tid / d.T, t = tid - slot * d.T;
+      if (slot == 0 || has1) {
+        float v = 0.f;
+        for (int w = 0; w < kCW; ++w) v += s.u.part[slot][w][t];
+        p.r.logits[(size_t)t * d.E + (slot ? e1 : e0)] = v;
+      }
+    }
+    cbar();
+  }
+  if (tid == 0) {
+    __threadfence();
+    s.flag = (atomicAdd(&p.sync[0], 1u) == gridDim.x - 1);
+  }
+  cbar();
+  if (!s.flag) return;
+  __threadfence();
+
+  // ---- this CTA scored last: top-k, histogram, scan, permutation, task lists
+  if (tid < kMaxExperts) s.counts_s[tid] = 0;
+  cbar();
+  for (int t = warp; t < d.T; t += kCW) {
+    for (int i = lane; i < d.E; i += 32) s.u.lbuf[warp][i] = __ldcg(p.r.logits + (size_t)t * d.E + i);
+    __syncwarp();
+    int id;
+    float w;
+    warp_topk(s.u.lbuf[warp], p.router_bias, d.E, d.k, lane, &id, &w);
+    __syncwarp();
+    if (lane < d.k) {
+      if (id < 0 || id >= d.E) {
+        atomicOr(p.r.err, kErrRange);
+        id = 0;
+      }
+      p.r.ids[t * d.k + lane] = id;
+      p.r.wts[t * d.k + lane] = w;
+      s.ids_s[t * d.k + lane] = id;
+      atomicAdd(&s.counts_s[id], 1);
+    }
+  }
+  cbar();
+  {
+    const int e = tid;
+    const int c = (e < d.E) ? s.counts_s[e] : 0;
+    const int ps = passes_of(c);
+    const int4 v = make_int4(c, c > 0 ? 1 : 0, ps * (d.I / kTile1), ps * (d.H / kTile2));
+    int4 tot;
+    const int4 ex = cscan4(v, s.scan, &tot);
+    if (e < d.E) {
+      s.offs_s[e] = ex.x;
+      p.r.offsets[e] = ex.x;
+      p.r.counts[e] = c;
+      if (c > 0) {
+        p.r.active[ex.y] = e;
+        p.r.task1[ex.y] = ex.z;
+        p.r.task2[ex.y] = ex.w;
+      }
+    }
+    if (tid == 0) {
+      p.r.offsets[d.E] = tot.x;
+      p.r.task1[tot.y] = tot.z;
+      p.r.task2[tot.y] = tot.w;
+      p.r.meta[kMetaActive] = tot.y;
+      p.r.meta[kMetaTasks1] = tot.z;
+      p.r.meta[kMetaTasks2] = tot.w;
+    }
+  }
+  cbar();
+  const int n = d.T * d.k;
+  for (int i = tid; i < n; i += kCW * 32) {
+    const int ei = s.ids_s[i];
+    int rank = 0;
+    for (int j = 0; j < i; ++j) rank += (s.ids_s[j] == ei);
+    const int pos = s.offs_s[ei] + rank;
+    p.r.perm[pos] = i / d.k;
+    p.r.inv[i] = pos;
+  }
+  cbar();
+  if (tid == 0) {
+    __threadfence();
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.sync + 1), "r"(1u) : "memory");
+  }
+}
+
+// ------------------------------------------------------------ the kernel
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tm13r, const __grid_constant__ CUtensorMap tm13s,
+                  const __grid_constant__ CUtensorMap tm2r, const __grid_constant__ CUtensorMap tm2s,
+                  const __grid_constant__ CUtensorMap ts13r, const __grid_constant__ CUtensorMap ts13s,
+                  const __grid_constant__ CUtensorMap ts2r, const __grid_constant__ CUtensorMap ts2s,
+                  const DecodeParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Dims& d = p.d;
+  unsigned* err = p.r.err;
+  const bool scale_tma = p.scale_tma != 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kS; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], kCW);
+    }
+    mbar_init(&s.bar[kBarRedFull], kCW);
+    mbar_init(&s.bar[kBarRedEmpty], kCW);
+    mbar_init(&s.bar[kBarDone], kCW);
+    mbar_init(&s.bar[kBarFlag], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  Counts cnt;
+  cnt.sh1 = d.Is > 0 ? (d.Is / kTile1) * passes_of(d.T) : 0;
+  cnt.sh2 = d.Is > 0 ? (d.H / kTile2) * passes_of(d.T) : 0;
+  cnt.r1 = cnt.r2 = cnt.n_act = 0;
+
+  if (warp == kCW) {
+    // ---------------------------------------------------------------- producer
+    bool known = false, stop = false;
+    int stage = 0;
+    uint32_t phase = 0;
+    // FIFO of stages whose h copies wait for their (expert, pass) counter
+    int pn = 0;
+    int q_stage[kS], q_g0[kS];
+    Task q_task[kS];
+
+    auto issue_acts = [&](int st_i, const Task& t, int g0) {
+      if (lane < t.nr) {
+        const int r = t.r0 + lane;
+        const uint16_t* src;
+        if (!t.down)
+          src = p.x + (size_t)(t.shared ? r - d.T * d.k : __ldcg(p.r.perm + r)) * d.H;
+        else
+          src = p.h + (size_t)r * p.hstride;
+        bulk_copy(smem_u32(s.stage[st_i] + kXO + lane * kXS), src + g0 * kGroup,
+                  min(8, t.ngroups - g0) * 256, &s.full[st_i]);
+      }
+    };
+    auto dep_ready = [&](const Task& t, bool block) -> int {
+      int ok = 1;
+      const int* c = p.done1 + t.e * kMaxPass + t.pass;
+      if (lane == 0)
+        ok = block ? (wait_counter(c, t.cnt_target, err) ? 1 : 0)
+                   : (ld_acquire(c) >= t.cnt_target ? 1 : 0);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (ok) {
+        // every lane that copies h orders its copies after the producers' writes
+        (void)ld_acquire(c);
+        fence_proxy_async();
+      }
+      return ok;
+    };
+    // issue h copies of queued stages whose dependency is met (oldest first)
+    auto drain = [&](bool block) -> bool {
+      while (pn > 0) {
+        const int ok = dep_ready(q_task[0], block);
+        if (!ok) {
+          if (block) return false;
+          break;
+        }
+        issue_acts(q_stage[0], q_task[0], q_g0[0]);
+        for (int i = 1; i < pn; ++i) {
+          q_stage[i - 1] = q_stage[i];
+          q_g0[i - 1] = q_g0[i];
+          q_task[i - 1] = q_task[i];
+        }
+        --pn;
+      }
+      return true;
+    };
+
+    for (int tau = blockIdx.x; !stop; tau += gridDim.x) {
+      if (tau >= cnt.sh1 + cnt.sh2 && !known) {
+        int ok = 1;
+        const int* ready = reinterpret_cast<const int*>(p.sync + 1);
+        if (lane == 0) ok = wait_counter(ready, 1, err) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        (void)ld_acquire(ready);  // routing was written by another CTA of this grid
+        cnt.n_act = __ldcg(p.r.meta + kMetaActive);
+        cnt.r1 = __ldcg(p.r.meta + kMetaTasks1);
+        cnt.r2 = __ldcg(p.r.meta + kMetaTasks2);
+        for (int i = lane; i <= cnt.n_act; i += 32) {
+          s.pre1[i] = __ldcg(p.r.task1 + i);
+          s.pre2[i] = __ldcg(p.r.task2 + i);
+          if (i < cnt.n_act) s.active[i] = __ldcg(p.r.active + i);
+        }
+        for (int i = lane; i <= d.E; i += 32) s.offsets[i] = __ldcg(p.r.offsets + i);
+        if (lane == 0) {
+          s.meta[0] = cnt.n_act;
+          s.meta[1] = cnt.r1;
+          s.meta[2] = cnt.r2;
+        }
+        __syncwarp();
+        known = true;
+      }
+      const Task t = task_at(s, d, cnt, tau);
+      if (t.ngroups == 0) break;
+      const CUtensorMap* tm = t.down ? (t.shared ? &tm2s : &tm2r) : (t.shared ? &tm13s : &tm13r);
+      const CUtensorMap* ts = t.down ? (t.shared ? &ts2s : &ts2r) : (t.shared ? &ts13s : &ts13r);
+      for (int g0 = 0; g0 < t.ngroups; g0 += 8) {
+        const int gcnt = min(8, t.ngroups - g0);
+        int ok = 1;
+        if (lane == 0) {
+          ok = dwait(&s.empty[stage], phase ^ 1u, err) ? 1 : 0;
+          if (ok) {
+            Desc& ds = s.desc[stage];
+            ds.flags = (g0 == 0 ? kFirst : 0) | (g0 + 8 >= t.ngroups ? kLast : 0) |
+                       (t.shared ? kShared : 0) | (t.down ? kDown : 0);
+            ds.g0 = g0;
+            ds.gcnt = gcnt;
+            ds.ngroups = t.ngroups;
+            ds.tile = t.tile;
+            ds.r0 = t.r0;
+            ds.nr = t.nr;
+            ds.rowA0 = t.rowA0;
+            ds.rowA1 = t.rowA1;
+            ds.cnt = t.e * kMaxPass + t.pass;
+            // a TMA box always delivers its full size (out-of-range parts are zero-filled)
+            mbar_arrive_expect_tx(&s.full[stage], kWB + (scale_tma ? kSB : 0) + t.nr * gcnt * 256);
+            uint8_t* st = s.stage[stage];
+            tma_2d(smem_u32(st), tm, &s.full[stage], g0 * 16, t.rowA0);
+            tma_2d(smem_u32(st + kWB / 2), tm, &s.full[stage], g0 * 16, t.rowA1);
+            if (scale_tma) {
+              tma_2d(smem_u32(st + kWB), ts, &s.full[stage], g0, t.rowA0);
+              tma_2d(smem_u32(st + kWB + kSB / 2), ts, &s.full[stage], g0, t.rowA1);
+            }
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          stop = true;
+          break;
+        }
+        if (!t.down) {
+          issue_acts(stage, t, g0);
+        } else {
+          q_stage[pn] = stage;
+          q_g0[pn] = g0;
+          q_task[pn] = t;
+          ++pn;
+          if (!drain(pn == kS)) {
+            stop = true;
+            break;
+          }
+        }
+        if (++stage == kS) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!stop) stop = !drain(true);
+    if (lane == 0 && !stop && dwait(&s.empty[stage], phase ^ 1u, err)) {
+      s.desc[stage].flags = kEnd;
+      mbar_arrive(&s.full[stage]);
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    router_phase(s, p);
+    const int g = lane >> 2, c = lane & 3;
+    const int gw = warp & 7, tl = warp >> 3;
+    const uint32_t stage0 = smem_u32(s.stage[0]);
+    const uint32_t w_off = tl * (kWB / 2) + g * 512 + gw * 64 + c * 16;
+    const uint32_t s_off = kWB + tl * (kSB / 2) + g * 16 + gw * 2;
+    const uint32_t x_off = kXO + g * kXS + gw * 256 + c * 64;
+    int stage = 0;
+    uint32_t phase = 0, tphase = 0;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (;;) {
+      if (!dwait(&s.full[stage], phase, err)) break;
+      const Desc ds = s.desc[stage];
+      if (ds.flags & kEnd) break;
+      if (ds.flags & kFirst) acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+      if (gw < ds.gcnt) {
+        const uint32_t st = stage0 + stage * kStageB;
+        const uint4 wA = lds128(st + w_off), wB = lds128(st + w_off + 8 * 512);
+        float s0, s1;
+        if (scale_tma) {
+          s0 = bf16_bits_to_f32(lds16(st + s_off));
+          s1 = bf16_bits_to_f32(lds16(st + s_off + 8 * 16));
+        } else {
+          const uint16_t* scl = (ds.flags & kDown) ? ((ds.flags & kShared) ? p.s2_shared : p.s2_routed)
+                                                   : ((ds.flags & kShared) ? p.s13_shared : p.s13_routed);
+          const int row = (tl ? ds.rowA1 : ds.rowA0) + g;
+          s0 = bf16_bits_to_f32(__ldg(scl + (size_t)row * ds.ngroups + ds.g0 + gw));
+          s1 = bf16_bits_to_f32(__ldg(scl + (size_t)(row + 8) * ds.ngroups + ds.g0 + gw));
+        }
+        uint4 b[4];
+        if (g < ds.nr) {
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            b[m] = lds128(st + x_off + m * 16);
+            if (!(ds.flags & kDown)) b[m] = interleave8(b[m]);
+          }
+        } else {
+#pragma unroll
+          for (int m = 0; m < 4; ++m) b[m] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        // 8 MMA steps in 4 independent chains
+        float t4[4][4] = {};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t ra = word_of(wA, m), rb = word_of(wB, m);
+          uint32_t a[4];
+          a[0] = int4_pair_to_bf16x2<0>(ra);
+          a[1] = int4_pair_to_bf16x2<0>(rb);
+          a[2] = int4_pair_to_bf16x2<1>(ra);
+          a[3] = int4_pair_to_bf16x2<1>(rb);
+          mma_bf16_16816(t4[(2 * m) & 3], a, b[m].x, b[m].y, t4[(2 * m) & 3]);
+          a[0] = int4_pair_to_bf16x2<2>(ra);
+          a[1] = int4_pair_to_bf16x2<2>(rb);
+          a[2] = int4_pair_to_bf16x2<3>(ra);
+          a[3] = int4_pair_to_bf16x2<3>(rb);
+          mma_bf16_16816(t4[(2 * m + 1) & 3], a, b[m].z, b[m].w, t4[(2 * m + 1) & 3]);
+        }
+        float tmp[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tmp[i] = (t4[0][i] + t4[1][i]) + (t4[2][i] + t4[3][i]);
+        acc[0] = fmaf(s0, tmp[0], acc[0]);
+        acc[1] = fmaf(s0, tmp[1], acc[1]);
+        acc[2] = fmaf(s1, tmp[2], acc[2]);
+        acc[3] = fmaf(s1, tmp[3], acc[3]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.empty[stage]);
+      if (++stage == kS) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      if (!(ds.flags & kLast)) continue;
+
+      // ---- end of a task: fixed-order cross-warp reduction and epilogue
+      if (!dwait(&s.bar[kBarRedEmpty], tphase ^ 1u, err)) break;
+      s.u.red[warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.bar[kBarRedFull]);
+      if (!dwait(&s.bar[kBarRedFull], tphase, err)) break;
+      const float* red = reinterpret_cast<const float*>(s.u.red);
+      const bool down = (ds.flags & kDown) != 0;
+      if (!down) {
+        if (threadIdx.x < 16 * kR) {
+          const int row = threadIdx.x >> 3, tok = threadIdx.x & 7;
+          const int ln = (row & 7) * 4 + (tok >> 1), q = (row >> 3) * 2 + (tok & 1);
+          float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            v0 += red[(w * 32 + ln) * 4 + q];
+            v1 += red[((8 + w) * 32 + ln) * 4 + q];
+          }
+          if (tok < ds.nr) {
+            const int n = ds.tile * kTile1 + row;
+            const int pos = (n & ~7) | ((n & 3) << 1) | ((n >> 2) & 1);
+            p.h[(size_t)(ds.r0 + tok) * p.hstride + pos] = f32_to_bf16_bits(silu(v0) * v1);
+          }
+        }
+      } else if (threadIdx.x < 2 * 16 * kR) {
+        const int tt = threadIdx.x >> 7, row = (threadIdx.x >> 3) & 15, tok = threadIdx.x & 7;
+        const int ln = (row & 7) * 4 + (tok >> 1), q = (row >> 3) * 2 + (tok & 1);
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) v += red[((tt * 8 + w) * 32 + ln) * 4 + q];
+        if (tok < ds.nr) p.y[(size_t)(ds.r0 + tok) * d.H + ds.tile * kTile2 + tt * 16 + row] = v;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&s.bar[kBarRedEmpty]);
+        mbar_arrive(&s.bar[kBarDone]);
+      }
+      if (threadIdx.x == 0) {
+        int f = 0;
+        if (dwait(&s.bar[kBarDone], tphase, err)) {
+          __threadfence();
+          if (!down) {
+            atomicAdd(p.done1 + ds.cnt, 1);
+          } else {
+            const int per_tile = (cnt.sh2 + s.meta[2]) / (d.H / kTile2);
+            f = (atomicAdd(p.tile_cnt + ds.tile, 1) == per_tile - 1);
+          }
+        }
+        s.flag = f;
+        mbar_arrive(&s.bar[kBarFlag]);
+      }
+      if (!dwait(&s.bar[kBarFlag], tphase, err)) break;
+      if (s.flag) {
+        // last down task of this channel tile: combine it for every token
+        __threadfence();
+        const int n0 = ds.tile * kTile2;
+        for (int i = threadIdx.x; i < d.T * kTile2; i += kCW * 32) {
+          const int tok = i / kTile2, n = n0 + (i - tok * kTile2);
+          float a = d.Is > 0 ? __ldcg(p.y + (size_t)(d.T * d.k + tok) * d.H + n) : 0.f;
+          for (int j = 0; j < d.k; ++j) {
+            const float w = __ldcg(p.r.wts + tok * d.k + j);
+            const int row = __ldcg(p.r.inv + tok * d.k + j);
+            a = fmaf(w, __ldcg(p.y + (size_t)row * d.H + n), a);
+          }
+          p.out[(size_t)tok * d.H + n] = f32_to_bf16_bits(a);
+        }
+      }
+      tphase ^= 1u;
+    }
+  }
+
+  // ---- the last CTA out resets the grid's counters for the next forward
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s.flag = (atomicAdd(&p.sync[2], 1u) == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (s.flag) {
+    __threadfence();
+    for (int i = threadIdx.x; i < (d.E + 1) * kMaxPass; i += blockDim.x) p.done1[i] = 0;
+    for (int i = threadIdx.x; i < d.H / kTile2; i += blockDim.x) p.tile_cnt[i] = 0;
+    if (threadIdx.x == 0) {
+      p.sync[0] = 0u;
+      p.sync[1] = 0u;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      p.sync[2] = 0u;
+    }
+  }
+}
+
+}  // namespace
+
+int decode_smem_bytes() { return (int)sizeof(Smem); }
+
+cudaError_t decode_setup(int* ctas_per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sizeof(Smem));
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_kernel, kThreads,
+                                                       sizeof(Smem));
+}
+
+size_t decode_counter_ints(int E, int H) { return (size_t)(E + 1) * kMaxPass + H / kTile2 + 4; }
+
+cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& w, const uint16_t* x,
+                          uint16_t* h, int hstride, float* y, uint16_t* out, int* counters, int grid,
+                          cudaStream_t s, LaunchLog& log) {
+  DecodeParams p{};
+  p.d = d;
+  p.r = r;
+  p.x = x;
+  p.router_w = w.router_w;
+  p.router_bias = w.router_bias;
+  p.s13_routed = w.s13_routed;
+  p.s13_shared = w.s13_shared;
+  p.s2_routed = w.s2_routed;
+  p.s2_shared = w.s2_shared;
+  p.h = h;
+  p.hstride = hstride;
+  p.y = y;
+  p.out = out;
+  p.done1 = counters;
+  p.tile_cnt = counters + (size_t)(d.E + 1) * kMaxPass;
+  p.sync = reinterpret_cast<unsigned*>(p.tile_cnt + d.H / kTile2);
+  p.scale_tma = w.scale_tma;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sizeof(Smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  log.begin("decode_fused", s);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel, w.tm13r, w.tm13s, w.tm2r, w.tm2s,
+                                     w.ts13r, w.ts13s, w.ts2r, w.ts2s, p);
+  log.end(s);
+  return e;
+}
+
+}  // namespace moe

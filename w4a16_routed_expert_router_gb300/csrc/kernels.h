@@ -56,6 +56,26 @@ cudaError_t launch_gemv_gate_up(const Dims& d, const Routing& r, const GemvWeigh
 cudaError_t launch_gemv_down(const Dims& d, const Routing& r, const GemvWeights& w,
                              const uint16_t* h, int hstride, float* y, uint16_t* out,
                              int* tile_cnt, int grid, cudaStream_t s, LaunchLog& log);
+// Decode-sized forward (T <= kSmallT) as one cooperative persistent kernel.
+struct DecodeWeights {
+  const float* router_w;
+  const float* router_bias;
+  const uint16_t* s13_routed;
+  const uint16_t* s13_shared;
+  const uint16_t* s2_routed;
+  const uint16_t* s2_shared;
+  // 2-D views of the packed weights {K/8 words, rows}, box {128 words, 16 rows}
+  CUtensorMap tm13r, tm13s, tm2r, tm2s;
+  // 2-D views of the scales {K/128, rows}, box {8, 16} (when scale_tma)
+  CUtensorMap ts13r, ts13s, ts2r, ts2s;
+  int scale_tma;
+};
+cudaError_t decode_setup(int* ctas_per_sm);
+size_t decode_counter_ints(int E, int H);
+cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& w, const uint16_t* x,
+                          uint16_t* h, int hstride, float* y, uint16_t* out, int* counters, int grid,
+                          cudaStream_t s, LaunchLog& log);
+
 cudaError_t launch_combine(const Dims& d, const Routing& r, const float* y, uint16_t* out,
                            cudaStream_t s, LaunchLog& log);
 

@@ -15,6 +15,8 @@ struct moe_w4a16_handle {
   int device = 0;
   int num_sms = 0;
   int gemv_grid = 0;
+  int decode_grid = 0;
+  int* counters = nullptr;      // decode kernel completion counters (self-resetting)
   void* ws = nullptr;
   size_t ws_bytes = 0;
   Routing r{};
@@ -29,9 +31,11 @@ struct moe_w4a16_handle {
   cudaEvent_t events[2 * LaunchLog::kMax];
   bool events_made = false;
   // tensor-map cache keyed by the tensor pointers it was encoded for:
-  // 0 w13_q, 1 w2_q, 2 sh_w13_q, 3 sh_w2_q, 4 w13_s, 5 w2_s, 6 sh_w13_s, 7 sh_w2_s
-  const void* map_keys[8] = {};
-  CUtensorMap maps[8];
+  // 0 w13_q, 1 w2_q, 2 sh_w13_q, 3 sh_w2_q (3-D, 1-group boxes), 4 w13_s, 5 w2_s,
+  // 6 sh_w13_s, 7 sh_w2_s (scales), 8 w13_q, 9 w2_q, 10 sh_w13_q, 11 sh_w2_q
+  // (2-D, 8-group boxes)
+  const void* map_keys[12] = {};
+  CUtensorMap maps[12];
 };
 
 namespace {
@@ -112,6 +116,7 @@ Layout plan(const moe_w4a16_config& c) {
       rows * H * 4,          // 17 y
       Tm * H * 2,            // 18 x_dev
       Tm * H * 2,            // 19 out_dev
+      decode_counter_ints(c.num_experts, c.hidden) * 4,  // 20 decode counters
   };
   Layout L;
   size_t o = 0;
@@ -168,10 +173,30 @@ int encode_scale_map(CUtensorMap* m, const void* base, long long rows, int K) {
   return MOE_W4A16_OK;
 }
 
+// 2-D view {K/8 words, rows} of a packed INT4 tensor [rows, K/8] uint32, box
+// {128 words, 16 rows}: 8 K-groups of 16 rows (8 KB).
+int encode_int4_map2d(CUtensorMap* m, const void* base, long long rows, int K) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MOE_W4A16_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)K / 8, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K / 2};
+  cuuint32_t box[2] = {128, 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    fprintf(stderr, "moe_w4a16: cuTensorMapEncodeTiled (2-D) failed (%d)\n", (int)r);
+    return MOE_W4A16_ERR_CUDA;
+  }
+  return MOE_W4A16_OK;
+}
+
 int get_map(moe_w4a16_handle* h, int slot, const void* base, long long rows, int K) {
   if (h->map_keys[slot] == base && base) return MOE_W4A16_OK;
-  const int st = slot < 4 ? encode_int4_map(&h->maps[slot], base, rows, K)
-                          : encode_scale_map(&h->maps[slot], base, rows, K);
+  const int st = slot < 4   ? encode_int4_map(&h->maps[slot], base, rows, K)
+                 : slot < 8 ? encode_scale_map(&h->maps[slot], base, rows, K)
+                            : encode_int4_map2d(&h->maps[slot], base, rows, K);
   if (st == MOE_W4A16_OK) h->map_keys[slot] = base;
   return st;
 }
@@ -246,6 +271,12 @@ int moe_w4a16_create(const moe_w4a16_config* cfg, int device, moe_w4a16_handle**
     return st != MOE_W4A16_OK ? st : MOE_W4A16_ERR_CUDA;
   }
   h->gemv_grid = h->num_sms * per_sm;
+  int dec_per_sm = 0;
+  if ((st = cuda_status(decode_setup(&dec_per_sm))) != MOE_W4A16_OK || dec_per_sm < 1) {
+    delete h;
+    return st != MOE_W4A16_OK ? st : MOE_W4A16_ERR_CUDA;
+  }
+  h->decode_grid = h->num_sms * dec_per_sm;
 
   const Layout L = plan(*cfg);
   if ((st = cuda_status(cudaMalloc(&h->ws, L.total))) != MOE_W4A16_OK) {
@@ -277,6 +308,7 @@ int moe_w4a16_create(const moe_w4a16_config* cfg, int device, moe_w4a16_handle**
   h->y = reinterpret_cast<float*>(b + L.off[17]);
   h->x_dev = reinterpret_cast<uint16_t*>(b + L.off[18]);
   h->out_dev = reinterpret_cast<uint16_t*>(b + L.off[19]);
+  h->counters = reinterpret_cast<int*>(b + L.off[20]);
 
   if (cfg->flags & MOE_W4A16_FLAG_PROFILE) {
     for (int i = 0; i < 2 * LaunchLog::kMax; ++i) cudaEventCreate(&h->events[i]);
@@ -363,18 +395,47 @@ int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t T, const m
   g2.scale_shared = has_sh ? w->sh_w2_s : w->w2_s;
   g2.scale_tma = scale_tma;
 
-  const bool fuse = T <= kSmallT;
   cudaError_t e;
+  if (T <= kSmallT) {
+    // decode sizes: the whole layer in one cooperative persistent kernel
+    if ((st = get_map(h, 8, w->w13_q, r13, c.hidden)) != MOE_W4A16_OK) return st;
+    if ((st = get_map(h, 9, w->w2_q, r2, c.inter)) != MOE_W4A16_OK) return st;
+    if (has_sh) {
+      if ((st = get_map(h, 10, w->sh_w13_q, 2LL * c.shared_inter, c.hidden)) != MOE_W4A16_OK)
+        return st;
+      if ((st = get_map(h, 11, w->sh_w2_q, c.hidden, c.shared_inter)) != MOE_W4A16_OK) return st;
+    }
+    DecodeWeights dw;
+    dw.router_w = w->router_w;
+    dw.router_bias = w->router_bias;
+    dw.s13_routed = w->w13_s;
+    dw.s13_shared = has_sh ? w->sh_w13_s : w->w13_s;
+    dw.s2_routed = w->w2_s;
+    dw.s2_shared = has_sh ? w->sh_w2_s : w->w2_s;
+    dw.tm13r = h->maps[8];
+    dw.tm13s = has_sh ? h->maps[10] : h->maps[8];
+    dw.tm2r = h->maps[9];
+    dw.tm2s = has_sh ? h->maps[11] : h->maps[9];
+    dw.ts13r = g1.ts_routed;
+    dw.ts13s = g1.ts_shared;
+    dw.ts2r = g2.ts_routed;
+    dw.ts2s = g2.ts_shared;
+    dw.scale_tma = scale_tma;
+    if ((e = launch_decode(d, h->r, dw, x, h->h, h->hstride, h->y, out, h->counters,
+                           h->decode_grid, s, h->log)) != cudaSuccess)
+      return cuda_status(e);
+    h->last_T = T;
+    return MOE_W4A16_OK;
+  }
   if ((e = launch_route(d, h->r, x, w->router_w, w->router_bias, s, h->log)) != cudaSuccess)
     return cuda_status(e);
   if ((e = launch_gemv_gate_up(d, h->r, g1, x, h->h, h->hstride, h->gemv_grid, s, h->log)) !=
       cudaSuccess)
     return cuda_status(e);
-  if ((e = launch_gemv_down(d, h->r, g2, h->h, h->hstride, h->y, fuse ? out : nullptr,
-                            h->tile_cnt, h->gemv_grid, s, h->log)) != cudaSuccess)
+  if ((e = launch_gemv_down(d, h->r, g2, h->h, h->hstride, h->y, nullptr, h->tile_cnt,
+                            h->gemv_grid, s, h->log)) != cudaSuccess)
     return cuda_status(e);
-  if (!fuse)
-    if ((e = launch_combine(d, h->r, h->y, out, s, h->log)) != cudaSuccess) return cuda_status(e);
+  if ((e = launch_combine(d, h->r, h->y, out, s, h->log)) != cudaSuccess) return cuda_status(e);
   h->last_T = T;
   return MOE_W4A16_OK;
 }
