@@ -609,6 +609,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* ts = t.down ? (t.shared ? &ts2s : &ts2r) : (t.shared ? &ts13s : &ts13r);
       for (int g0 = 0; g0 < t.ngroups; g0 += 8) {
         const int gcnt = min(8, t.ngroups - g0);
+        // Consumers take stages in ring order: a queued down stage whose h
+        // copies are not issued yet holds every later stage back. Resolve the
+        // queue (blocking on the oldest dependency, which only needs earlier
+        // gate/up tasks) before waiting for a slot that is not free yet.
+        if (pn > 0 && !drain(false)) {
+          stop = true;
+          break;
+        }
+        if (pn > 0) {
+          int free_slot = 0;
+          if (lane == 0) free_slot = mbar_try_wait(&s.empty[stage], phase ^ 1u) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, free_slot, 0) && !drain(true)) {
+            stop = true;
+            break;
+          }
+        }
         int ok = 1;
         if (lane == 0) {
           ok = dwait(&s.empty[stage], phase ^ 1u, err) ? 1 : 0;
@@ -647,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           q_g0[pn] = g0;
           q_task[pn] = t;
           ++pn;
-          if (!drain(pn == kS)) {
+          if (!drain(false)) {
             stop = true;
             break;
           }
