@@ -29,9 +29,13 @@
 //  * 16 consumer warps: warp w takes K-group (w % 8) of tile (w / 8) of every
 //    stage; exact INT4 -> bf16 in registers, mma.sync m16n8k16 with weights as
 //    A and up to 8 rows as B, group scales applied in fp32.
-//  * Gate/up epilogue: SwiGLU -> bf16 h, then +1 on the (expert, pass)
-//    counter. Down epilogue: fp32 y; the last task of a channel tile combines
-//    the tile for every token (out = y_shared + sum_j w_j y_j, slot order).
+//  * Task ends need no rendezvous: each warp drops its partial sums into one
+//    of two task slots and the last warp to arrive reduces them in fixed warp
+//    order and runs the epilogue while the others keep consuming stages.
+//    Gate/up epilogue: SwiGLU -> bf16 h, then a release-add on the (expert,
+//    pass) counter. Down epilogue: fp32 y; the warp whose task completes a
+//    channel tile (acq_rel ticket) combines the tile for every token
+//    (out = y_shared + sum_j w_j y_j, slot order).
 //  * Every wait is bounded in time and gives up once any wait of the grid has
 //    timed out (device error flag), so a broken hand-off cannot hang the GPU.
 //    The grid is launched cooperatively so all CTAs are co-resident; every
@@ -61,15 +65,14 @@ struct Desc {
   int flags, g0, gcnt, ngroups, tile, r0, nr, rowA0, rowA1, cnt, pad[2];
 };
 
-enum { kBarRedFull = 0, kBarRedEmpty, kBarDone, kBarFlag, kNumBars };
-
 struct Smem {
   uint8_t stage[kS][kStageB];
   union {
-    float4 red[kCW * 32];               // task-end partial sums
+    float4 red2[2][kCW * 32];           // task-end partial sums, two task slots
     float part[2][kCW][kSmallT];        // router: per-warp partial logits of 2 experts
     float lbuf[kCW][kMaxExperts];       // router finish: one token's logits per warp
   } u;
+  int red_cnt[2];
   int ids_s[kSmallT * kMaxTopK];
   int counts_s[kMaxExperts];
   int offs_s[kMaxExperts];
@@ -82,7 +85,7 @@ struct Smem {
   int meta[4];                          // n_act, routed gate/up tasks, routed down tasks
   uint64_t full[kS];
   uint64_t empty[kS];
-  uint64_t bar[kNumBars];
+  uint64_t red_free[2];
   int flag;
 };
 
@@ -511,10 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], kCW);
     }
-    mbar_init(&s.bar[kBarRedFull], kCW);
-    mbar_init(&s.bar[kBarRedEmpty], kCW);
-    mbar_init(&s.bar[kBarDone], kCW);
-    mbar_init(&s.bar[kBarFlag], 1);
+    mbar_init(&s.red_free[0], 1);
+    mbar_init(&s.red_free[1], 1);
+    s.red_cnt[0] = s.red_cnt[1] = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -689,7 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_off = kWB + tl * (kSB / 2) + g * 16 + gw * 2;
     const uint32_t x_off = kXO + g * kXS + gw * 256 + c * 64;
     int stage = 0;
-    uint32_t phase = 0, tphase = 0;
+    uint32_t phase = 0;
+    int tseq = 0;  // tasks finished by this warp (the same sequence for all warps)
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (;;) {
       if (!dwait(&s.full[stage], phase, err)) break;
@@ -754,63 +757,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!(ds.flags & kLast)) continue;
 
-      // ---- end of a task: fixed-order cross-warp reduction and epilogue
-      if (!dwait(&s.bar[kBarRedEmpty], tphase ^ 1u, err)) break;
-      s.u.red[warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      // ---- end of a task: each warp drops its partial sums into the task's
+      // slot; the last warp to arrive reduces them (fixed warp order) and
+      // runs the epilogue while the other warps move on.
+      const int bsel = tseq & 1;
+      if (!dwait(&s.red_free[bsel], ((tseq >> 1) & 1) ^ 1u, err)) break;
+      s.u.red2[bsel][warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.bar[kBarRedFull]);
-      if (!dwait(&s.bar[kBarRedFull], tphase, err)) break;
-      const float* red = reinterpret_cast<const float*>(s.u.red);
-      const bool down = (ds.flags & kDown) != 0;
-      if (!down) {
-        if (threadIdx.x < 16 * kR) {
-          const int row = threadIdx.x >> 3, tok = threadIdx.x & 7;
-          const int ln = (row & 7) * 4 + (tok >> 1), q = (row >> 3) * 2 + (tok & 1);
-          float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-          for (int w = 0; w < 8; ++w) {
-            v0 += red[(w * 32 + ln) * 4 + q];
-            v1 += red[((8 + w) * 32 + ln) * 4 + q];
-          }
-          if (tok < ds.nr) {
-            const int n = ds.tile * kTile1 + row;
-            const int pos = (n & ~7) | ((n & 3) << 1) | ((n >> 2) & 1);
-            p.h[(size_t)(ds.r0 + tok) * p.hstride + pos] = f32_to_bf16_bits(silu(v0) * v1);
-          }
-        }
-      } else if (threadIdx.x < 2 * 16 * kR) {
-        const int tt = threadIdx.x >> 7, row = (threadIdx.x >> 3) & 15, tok = threadIdx.x & 7;
-        const int ln = (row & 7) * 4 + (tok >> 1), q = (row >> 3) * 2 + (tok & 1);
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) v += red[((tt * 8 + w) * 32 + ln) * 4 + q];
-        if (tok < ds.nr) p.y[(size_t)(ds.r0 + tok) * d.H + ds.tile * kTile2 + tt * 16 + row] = v;
-      }
-      __syncwarp();
+      int last = 0;
       if (lane == 0) {
-        mbar_arrive(&s.bar[kBarRedEmpty]);
-        mbar_arrive(&s.bar[kBarDone]);
+        __threadfence_block();
+        last = atomicAdd(&s.red_cnt[bsel], 1) == kCW - 1;
+        if (last) s.red_cnt[bsel] = 0;
       }
-      if (threadIdx.x == 0) {
-        int f = 0;
-        if (dwait(&s.bar[kBarDone], tphase, err)) {
-          __threadfence();
-          if (!down) {
-            atomicAdd(p.done1 + ds.cnt, 1);
-          } else {
-            const int per_tile = (cnt.sh2 + s.meta[2]) / (d.H / kTile2);
-            f = (atomicAdd(p.tile_cnt + ds.tile, 1) == per_tile - 1);
-          }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      ++tseq;
+      if (!last) continue;
+      __threadfence_block();
+      const float4* red = s.u.red2[bsel];
+      const bool down = (ds.flags & kDown) != 0;
+      // lane L holds the fragment (rows g, g+8) x (tokens 2c, 2c+1) of both tiles
+      float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float4 a = red[w * 32 + lane], bq = red[(8 + w) * 32 + lane];
+        v0.x += a.x; v0.y += a.y; v0.z += a.z; v0.w += a.w;
+        v1.x += bq.x; v1.y += bq.y; v1.z += bq.z; v1.w += bq.w;
+      }
+      const float f0[4] = {v0.x, v0.y, v0.z, v0.w}, f1[4] = {v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int row = g + 8 * (q >> 1), tok = 2 * c + (q & 1);
+        if (tok >= ds.nr) continue;
+        const size_t orow = (size_t)(ds.r0 + tok);
+        if (!down) {
+          const int n = ds.tile * kTile1 + row;
+          const int pos = (n & ~7) | ((n & 3) << 1) | ((n >> 2) & 1);
+          p.h[orow * p.hstride + pos] = f32_to_bf16_bits(silu(f0[q]) * f1[q]);
+        } else {
+          float* yr = p.y + orow * d.H + ds.tile * kTile2;
+          yr[row] = f0[q];
+          yr[16 + row] = f1[q];
         }
-        s.flag = f;
-        mbar_arrive(&s.bar[kBarFlag]);
       }
-      if (!dwait(&s.bar[kBarFlag], tphase, err)) break;
-      if (s.flag) {
+      __syncwarp();
+      int tile_last = 0;
+      if (lane == 0) {
+        if (!down) {
+          asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.done1 + ds.cnt) : "memory");
+        } else {
+          const int per_tile = (cnt.sh2 + s.meta[2]) / (d.H / kTile2);
+          int old;
+          asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                       : "=r"(old)
+                       : "l"(p.tile_cnt + ds.tile)
+                       : "memory");
+          tile_last = old == per_tile - 1;
+        }
+      }
+      tile_last = __shfl_sync(0xffffffffu, tile_last, 0);
+      if (tile_last) {
         // last down task of this channel tile: combine it for every token
         __threadfence();
         const int n0 = ds.tile * kTile2;
-        for (int i = threadIdx.x; i < d.T * kTile2; i += kCW * 32) {
+        for (int i = lane; i < d.T * kTile2; i += 32) {
           const int tok = i / kTile2, n = n0 + (i - tok * kTile2);
           float a = d.Is > 0 ? __ldcg(p.y + (size_t)(d.T * d.k + tok) * d.H + n) : 0.f;
           for (int j = 0; j < d.k; ++j) {
@@ -820,8 +830,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           p.out[(size_t)tok * d.H + n] = f32_to_bf16_bits(a);
         }
+        if (lane == 0) p.tile_cnt[ds.tile] = 0;
       }
-      tphase ^= 1u;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.red_free[bsel]);
     }
   }
 
