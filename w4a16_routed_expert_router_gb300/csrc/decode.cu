@@ -6,8 +6,8 @@
 // expert weights plus the 4 MB fp32 router at one token ("Throughputmaxxing:
 // DeepSeek-V4-Flash on Isambard-AI", "A pass through the model": below the
 // ridge the expert GEMMs are memory bound; "Where does the time go?": the
-// act+quant bucket is hundreds of tiny launches). Each kernel boundary costs a
-// ramp-up and a tail of the memory pipeline, so the whole layer runs as one
+// act+quant bucket is hundreds of tiny launches). Every kernel boundary costs
+// a ramp-up and a tail of the memory pipeline, so the whole layer runs as one
 // task stream that never stops fetching weights:
 //
 //   [gate/up shared | down shared | gate/up routed | down routed]
@@ -16,31 +16,33 @@
 // two 16-row weight tiles (16 gate + 16 up channels, or 32 down channels) of
 // one expert over all of K, for one pass of <= 8 rows of that expert.
 //
-//  * Router: consumer warps of every CTA first score one or two experts for
-//    all tokens (fp32). The CTA that finishes last (atomic ticket) runs top-k,
-//    histogram, scan, the stable permutation and the task lists, then
-//    publishes a ready flag. The shared expert's tasks need no routing and
-//    keep the memory system busy meanwhile.
-//  * Producer warp: decodes tasks, fills a 6-stage ring (2-D TMA boxes of 16
-//    rows x 512 B per tile, scale boxes, bulk copies of the activation rows)
-//    and hands each stage a descriptor. Down tasks need the h rows of their
+// Warp roles (one CTA per SM):
+//  * 16 consumer warps. First the router: every CTA scores one or two experts
+//    for all tokens (fp32), publishes the logits, waits until every CTA has
+//    (a counter), then computes the whole routing itself in shared memory
+//    (top-k, histogram, scan, stable permutation, task lists). Computing it
+//    redundantly per CTA keeps the critical path at two global round trips.
+//    Then the consumers stream stages: warp w takes K-group (w % 8) of tile
+//    (w / 8); exact INT4 -> bf16 in registers, mma.sync m16n8k16 with weights
+//    as A and up to 8 rows as B, group scales applied in fp32. At the end of
+//    a task each warp drops its partial sums into a slot and moves on.
+//  * 1 producer warp: decodes tasks and fills a 5-stage ring (2-D TMA boxes
+//    of 16 rows x 512 B per tile, scale boxes, bulk copies of the activation
+//    rows) with a descriptor per stage. Down tasks need the h rows of their
 //    (expert, pass): their weights are prefetched at once, their h copies wait
 //    on a per-(expert, pass) completion counter.
-//  * 16 consumer warps: warp w takes K-group (w % 8) of tile (w / 8) of every
-//    stage; exact INT4 -> bf16 in registers, mma.sync m16n8k16 with weights as
-//    A and up to 8 rows as B, group scales applied in fp32.
-//  * Task ends need no rendezvous: each warp drops its partial sums into one
-//    of two task slots and the last warp to arrive reduces them in fixed warp
-//    order and runs the epilogue while the others keep consuming stages.
-//    Gate/up epilogue: SwiGLU -> bf16 h, then a release-add on the (expert,
-//    pass) counter. Down epilogue: fp32 y; the warp whose task completes a
-//    channel tile (acq_rel ticket) combines the tile for every token
-//    (out = y_shared + sum_j w_j y_j, slot order).
+//  * 4 epilogue warps, one per slot: fixed-order reduction of the 16 partial
+//    sums, SwiGLU -> bf16 h (then a release-add on the (expert, pass)
+//    counter) or fp32 y (then an acq_rel ticket per channel tile; the task
+//    that completes a tile combines it for every token:
+//    out = y_shared + sum_j w_j y_j in slot order). Fences and atomics stay
+//    off the consumers' path.
 //  * Every wait is bounded in time and gives up once any wait of the grid has
 //    timed out (device error flag), so a broken hand-off cannot hang the GPU.
 //    The grid is launched cooperatively so all CTAs are co-resident; every
-//    CTA finishes all its gate/up tasks before any down task, so waits on
-//    counters always make progress. The last CTA to exit resets the counters.
+//    CTA finishes all its gate/up tasks before the down tasks that depend on
+//    them, so waits on counters always make progress. The last CTA to exit
+//    resets the counters.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -49,15 +51,18 @@ namespace moe {
 namespace {
 
 constexpr int kCW = 16;                      // consumer warps
-constexpr int kThreads = (kCW + 1) * 32;     // + one producer warp
+constexpr int kEW = 4;                       // epilogue warps (= slots)
+constexpr int kProd = kCW;                   // producer warp index
+constexpr int kThreads = (kCW + 1 + kEW) * 32;
 constexpr int kR = 8;                        // rows per pass (MMA N)
-constexpr int kS = 6;                        // ring stages
+constexpr int kS = 5;                        // ring stages
 constexpr int kWB = 2 * 16 * 512;            // 2 tiles x 16 rows x 512 B (8 K-groups)
 constexpr int kSB = 2 * 16 * 16;             // 2 tiles x 16 rows x 8 bf16 scales
 constexpr int kXS = 8 * 256 + 64;            // one activation row (8 groups bf16) + pad
 constexpr int kXO = kWB + kSB;
 constexpr int kStageB = (kXO + kR * kXS + 1023) / 1024 * 1024;
 constexpr int kMaxPass = (kSmallT + kR - 1) / kR;  // passes per expert at most
+constexpr int kItems = kSmallT * kMaxTopK;
 
 enum { kFirst = 1, kLast = 2, kEnd = 4, kShared = 8, kDown = 16 };
 
@@ -68,24 +73,27 @@ struct Desc {
 struct Smem {
   uint8_t stage[kS][kStageB];
   union {
-    float4 red2[2][kCW * 32];           // task-end partial sums, two task slots
+    float4 red[kEW][kCW * 32];          // task-end partial sums, one slot per epilogue warp
     float part[2][kCW][kSmallT];        // router: per-warp partial logits of 2 experts
-    float lbuf[kCW][kMaxExperts];       // router finish: one token's logits per warp
   } u;
-  int red_cnt[2];
-  int ids_s[kSmallT * kMaxTopK];
-  int counts_s[kMaxExperts];
-  int offs_s[kMaxExperts];
-  int4 scan[kCW];
+  Desc slot_desc[kEW];
   Desc desc[kS];
+  int ids_s[kItems];
+  float wts_s[kItems];
+  int perm_s[kItems];
+  int inv_s[kItems];
+  int counts_s[kMaxExperts];
   int active[kMaxExperts + 2];
   int pre1[kMaxExperts + 2];
   int pre2[kMaxExperts + 2];
   int offsets[kMaxExperts + 2];
+  int4 scan[kCW];
   int meta[4];                          // n_act, routed gate/up tasks, routed down tasks
   uint64_t full[kS];
   uint64_t empty[kS];
-  uint64_t red_free[2];
+  uint64_t slot_full[kEW];
+  uint64_t slot_free[kEW];
+  uint64_t route_ready;
   int flag;
 };
 
@@ -105,7 +113,7 @@ struct DecodeParams {
   uint16_t* out;                // [T, H] bf16
   int* done1;                   // [(E + 1) * kMaxPass] gate/up tasks done per (expert, pass)
   int* tile_cnt;                // [H / 32] down tasks done per channel tile
-  unsigned* sync;               // [4]: router ticket, ready flag, exit ticket
+  unsigned* sync;               // [4]: logits ticket, (unused), exit ticket
   int scale_tma;
 };
 
@@ -116,6 +124,7 @@ struct Task {
 
 __device__ __forceinline__ int passes_of(int rows) { return (rows + kR - 1) / kR; }
 
+// named barrier of the 512 consumer threads
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
 __device__ __forceinline__ bool aborted(const unsigned* err) {
@@ -149,7 +158,7 @@ __device__ __forceinline__ bool wait_counter(const int* p, int target, unsigned*
   if (ld_acquire(p) >= target) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
-    __nanosleep(64);
+    __nanosleep(32);
     if (ld_acquire(p) >= target) return true;
     if (aborted(err)) return false;
     if (global_ns() - t0 > kWaitLimitNs) {
@@ -267,6 +276,9 @@ __device__ __forceinline__ Task task_at(const Smem& s, const Dims& d, const Coun
 }
 
 // ------------------------------------------------------------ router (consumers)
+// Top-k of one token from its logits in global memory (lane l holds experts
+// l, l+32, ...); lanes 0..k-1 return the chosen expert (descending sel, ties
+// -> lower index) and its renormalised unbiased score.
 __device__ __forceinline__ void warp_topk(const float* logit_row, const float* bias, int E, int k,
                                           int lane, int* out_id, float* out_w) {
   constexpr int kPer = kMaxExperts / 32;
@@ -274,12 +286,16 @@ __device__ __forceinline__ void warp_topk(const float* logit_row, const float* b
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int e = lane + 32 * i;
+    sc[i] = (e < E) ? __ldcg(logit_row + e) : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
     if (e < E) {
-      const float s = 1.0f / (1.0f + expf(-logit_row[e]));
+      const float s = 1.0f / (1.0f + expf(-sc[i]));
       sc[i] = s;
-      sel[i] = s + bias[e];
+      sel[i] = s + __ldg(bias + e);
     } else {
-      sc[i] = 0.f;
       sel[i] = -INFINITY;
     }
   }
@@ -361,8 +377,9 @@ __device__ __forceinline__ int4 cscan4(int4 v, int4* scr, int4* total) {
                    base.w + inc.w - v.w);
 }
 
-// Consumer warps: score this CTA's experts; the last CTA finishes the routing.
-__device__ void router_phase(Smem& s, const DecodeParams& p) {
+// Consumer warps: score this CTA's experts, wait for every CTA's logits, then
+// compute the whole routing in shared memory. Returns false on timeout.
+__device__ bool router_phase(Smem& s, const DecodeParams& p) {
   const Dims& d = p.d;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kw = d.H / kCW;  // K slice of one warp
@@ -422,32 +439,29 @@ __device__ void router_phase(Smem& s, const DecodeParams& p) {
     }
     cbar();
   }
+  // publish this CTA's logits and wait for everybody's
   if (tid == 0) {
     __threadfence();
-    s.flag = (atomicAdd(&p.sync[0], 1u) == gridDim.x - 1);
+    atomicAdd(&p.sync[0], 1u);
+    s.flag = wait_counter(reinterpret_cast<const int*>(p.sync), (int)gridDim.x, p.r.err) ? 1 : 0;
   }
-  cbar();
-  if (!s.flag) return;
-  __threadfence();
-
-  // ---- this CTA scored last: top-k, histogram, scan, permutation, task lists
   if (tid < kMaxExperts) s.counts_s[tid] = 0;
   cbar();
+  if (!s.flag) return false;
+  (void)ld_acquire(reinterpret_cast<const int*>(p.sync));
+
+  // ---- the routing of every token, in shared memory
   for (int t = warp; t < d.T; t += kCW) {
-    for (int i = lane; i < d.E; i += 32) s.u.lbuf[warp][i] = __ldcg(p.r.logits + (size_t)t * d.E + i);
-    __syncwarp();
     int id;
     float w;
-    warp_topk(s.u.lbuf[warp], p.router_bias, d.E, d.k, lane, &id, &w);
-    __syncwarp();
+    warp_topk(p.r.logits + (size_t)t * d.E, p.router_bias, d.E, d.k, lane, &id, &w);
     if (lane < d.k) {
       if (id < 0 || id >= d.E) {
         atomicOr(p.r.err, kErrRange);
         id = 0;
       }
-      p.r.ids[t * d.k + lane] = id;
-      p.r.wts[t * d.k + lane] = w;
       s.ids_s[t * d.k + lane] = id;
+      s.wts_s[t * d.k + lane] = w;
       atomicAdd(&s.counts_s[id], 1);
     }
   }
@@ -460,22 +474,20 @@ __device__ void router_phase(Smem& s, const DecodeParams& p) {
     int4 tot;
     const int4 ex = cscan4(v, s.scan, &tot);
     if (e < d.E) {
-      s.offs_s[e] = ex.x;
-      p.r.offsets[e] = ex.x;
-      p.r.counts[e] = c;
+      s.offsets[e] = ex.x;
       if (c > 0) {
-        p.r.active[ex.y] = e;
-        p.r.task1[ex.y] = ex.z;
-        p.r.task2[ex.y] = ex.w;
+        s.active[ex.y] = e;
+        s.pre1[ex.y] = ex.z;
+        s.pre2[ex.y] = ex.w;
       }
     }
     if (tid == 0) {
-      p.r.offsets[d.E] = tot.x;
-      p.r.task1[tot.y] = tot.z;
-      p.r.task2[tot.y] = tot.w;
-      p.r.meta[kMetaActive] = tot.y;
-      p.r.meta[kMetaTasks1] = tot.z;
-      p.r.meta[kMetaTasks2] = tot.w;
+      s.offsets[d.E] = tot.x;
+      s.pre1[tot.y] = tot.z;
+      s.pre2[tot.y] = tot.w;
+      s.meta[0] = tot.y;
+      s.meta[1] = tot.z;
+      s.meta[2] = tot.w;
     }
   }
   cbar();
@@ -484,15 +496,36 @@ __device__ void router_phase(Smem& s, const DecodeParams& p) {
     const int ei = s.ids_s[i];
     int rank = 0;
     for (int j = 0; j < i; ++j) rank += (s.ids_s[j] == ei);
-    const int pos = s.offs_s[ei] + rank;
-    p.r.perm[pos] = i / d.k;
-    p.r.inv[i] = pos;
+    const int pos = s.offsets[ei] + rank;
+    s.perm_s[pos] = i / d.k;
+    s.inv_s[i] = pos;
   }
   cbar();
-  if (tid == 0) {
-    __threadfence();
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.sync + 1), "r"(1u) : "memory");
+  if (tid == 0) mbar_arrive(&s.route_ready);
+  // one CTA also writes the routing out (the get-routing hook reads it)
+  if (blockIdx.x == 0) {
+    for (int i = tid; i < n; i += kCW * 32) {
+      p.r.ids[i] = s.ids_s[i];
+      p.r.wts[i] = s.wts_s[i];
+      p.r.perm[i] = s.perm_s[i];
+      p.r.inv[i] = s.inv_s[i];
+    }
+    for (int e = tid; e <= d.E; e += kCW * 32) {
+      p.r.offsets[e] = s.offsets[e];
+      if (e < d.E) p.r.counts[e] = s.counts_s[e];
+    }
+    for (int a = tid; a <= s.meta[0]; a += kCW * 32) {
+      if (a < s.meta[0]) p.r.active[a] = s.active[a];
+      p.r.task1[a] = s.pre1[a];
+      p.r.task2[a] = s.pre2[a];
+    }
+    if (tid == 0) {
+      p.r.meta[kMetaActive] = s.meta[0];
+      p.r.meta[kMetaTasks1] = s.meta[1];
+      p.r.meta[kMetaTasks2] = s.meta[2];
+    }
   }
+  return true;
 }
 
 // ------------------------------------------------------------ the kernel
@@ -514,9 +547,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], kCW);
     }
-    mbar_init(&s.red_free[0], 1);
-    mbar_init(&s.red_free[1], 1);
-    s.red_cnt[0] = s.red_cnt[1] = 0;
+    for (int i = 0; i < kEW; ++i) {
+      mbar_init(&s.slot_full[i], kCW);
+      mbar_init(&s.slot_free[i], 1);
+    }
+    mbar_init(&s.route_ready, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -526,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cnt.sh2 = d.Is > 0 ? (d.H / kTile2) * passes_of(d.T) : 0;
   cnt.r1 = cnt.r2 = cnt.n_act = 0;
 
-  if (warp == kCW) {
+  if (warp == kProd) {
     // ---------------------------------------------------------------- producer
     bool known = false, stop = false;
     int stage = 0;
@@ -541,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = t.r0 + lane;
         const uint16_t* src;
         if (!t.down)
-          src = p.x + (size_t)(t.shared ? r - d.T * d.k : __ldcg(p.r.perm + r)) * d.H;
+          src = p.x + (size_t)(t.shared ? r - d.T * d.k : s.perm_s[r]) * d.H;
         else
           src = p.h + (size_t)r * p.hstride;
         bulk_copy(smem_u32(s.stage[st_i] + kXO + lane * kXS), src + g0 * kGroup,
@@ -581,28 +616,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
+    if (lane == 0) {
+      prefetch_tmap(&tm13r);
+      prefetch_tmap(&tm13s);
+      prefetch_tmap(&tm2r);
+      prefetch_tmap(&tm2s);
+    }
     for (int tau = blockIdx.x; !stop; tau += gridDim.x) {
       if (tau >= cnt.sh1 + cnt.sh2 && !known) {
+        // routed tasks: wait for this CTA's routing (shared memory)
         int ok = 1;
-        const int* ready = reinterpret_cast<const int*>(p.sync + 1);
-        if (lane == 0) ok = wait_counter(ready, 1, err) ? 1 : 0;
+        if (lane == 0) ok = dwait(&s.route_ready, 0, err) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        (void)ld_acquire(ready);  // routing was written by another CTA of this grid
-        cnt.n_act = __ldcg(p.r.meta + kMetaActive);
-        cnt.r1 = __ldcg(p.r.meta + kMetaTasks1);
-        cnt.r2 = __ldcg(p.r.meta + kMetaTasks2);
-        for (int i = lane; i <= cnt.n_act; i += 32) {
-          s.pre1[i] = __ldcg(p.r.task1 + i);
-          s.pre2[i] = __ldcg(p.r.task2 + i);
-          if (i < cnt.n_act) s.active[i] = __ldcg(p.r.active + i);
-        }
-        for (int i = lane; i <= d.E; i += 32) s.offsets[i] = __ldcg(p.r.offsets + i);
-        if (lane == 0) {
-          s.meta[0] = cnt.n_act;
-          s.meta[1] = cnt.r1;
-          s.meta[2] = cnt.r2;
-        }
-        __syncwarp();
+        cnt.n_act = s.meta[0];
+        cnt.r1 = s.meta[1];
+        cnt.r2 = s.meta[2];
         known = true;
       }
       const Task t = task_at(s, d, cnt, tau);
@@ -615,16 +643,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // copies are not issued yet holds every later stage back. Resolve the
         // queue (blocking on the oldest dependency, which only needs earlier
         // gate/up tasks) before waiting for a slot that is not free yet.
-        if (pn > 0 && !drain(false)) {
-          stop = true;
-          break;
-        }
         if (pn > 0) {
-          int free_slot = 0;
-          if (lane == 0) free_slot = mbar_try_wait(&s.empty[stage], phase ^ 1u) ? 1 : 0;
-          if (!__shfl_sync(0xffffffffu, free_slot, 0) && !drain(true)) {
-            stop = true;
-            break;
+          drain(false);
+          if (pn > 0) {
+            int free_slot = 0;
+            if (lane == 0) free_slot = mbar_try_wait(&s.empty[stage], phase ^ 1u) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, free_slot, 0) && !drain(true)) {
+              stop = true;
+              break;
+            }
           }
         }
         int ok = 1;
@@ -665,10 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           q_g0[pn] = g0;
           q_task[pn] = t;
           ++pn;
-          if (!drain(false)) {
-            stop = true;
-            break;
-          }
+          drain(false);
         }
         if (++stage == kS) {
           stage = 0;
@@ -681,9 +705,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       s.desc[stage].flags = kEnd;
       mbar_arrive(&s.full[stage]);
     }
-  } else {
+  } else if (warp < kCW) {
     // ---------------------------------------------------------------- consumers
-    router_phase(s, p);
+    const bool routed = router_phase(s, p);
     const int g = lane >> 2, c = lane & 3;
     const int gw = warp & 7, tl = warp >> 3;
     const uint32_t stage0 = smem_u32(s.stage[0]);
@@ -692,9 +716,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t x_off = kXO + g * kXS + gw * 256 + c * 64;
     int stage = 0;
     uint32_t phase = 0;
-    int tseq = 0;  // tasks finished by this warp (the same sequence for all warps)
+    int tseq = 0;  // tasks finished (the same sequence for all consumer warps)
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (;;) {
+    for (; routed;) {
       if (!dwait(&s.full[stage], phase, err)) break;
       const Desc ds = s.desc[stage];
       if (ds.flags & kEnd) break;
@@ -756,34 +780,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         phase ^= 1u;
       }
       if (!(ds.flags & kLast)) continue;
-
-      // ---- end of a task: each warp drops its partial sums into the task's
-      // slot; the last warp to arrive reduces them (fixed warp order) and
-      // runs the epilogue while the other warps move on.
-      const int bsel = tseq & 1;
-      if (!dwait(&s.red_free[bsel], ((tseq >> 1) & 1) ^ 1u, err)) break;
-      s.u.red2[bsel][warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      // end of a task: hand the partial sums to the slot's epilogue warp
+      const int b = tseq % kEW;
+      const uint32_t use = (uint32_t)(tseq / kEW);
+      if (!dwait(&s.slot_free[b], (use & 1u) ^ 1u, err)) break;
+      s.u.red[b][warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      if (warp == 0 && lane == 0) s.slot_desc[b] = ds;
       __syncwarp();
-      int last = 0;
-      if (lane == 0) {
-        __threadfence_block();
-        last = atomicAdd(&s.red_cnt[bsel], 1) == kCW - 1;
-        if (last) s.red_cnt[bsel] = 0;
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
+      if (lane == 0) mbar_arrive(&s.slot_full[b]);
       ++tseq;
-      if (!last) continue;
-      __threadfence_block();
-      const float4* red = s.u.red2[bsel];
+    }
+    // end of work: one end marker per epilogue warp
+    for (int j = 0; j < kEW; ++j) {
+      const int b = (tseq + j) % kEW;
+      const uint32_t use = (uint32_t)((tseq + j) / kEW);
+      if (!dwait(&s.slot_free[b], (use & 1u) ^ 1u, err)) break;
+      if (warp == 0 && lane == 0) s.slot_desc[b].flags = kEnd;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.slot_full[b]);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int b = warp - kCW - 1;  // this warp's slot
+    const int g = lane >> 2, c = lane & 3;
+    int routed_down = -1;
+    for (uint32_t use = 0;; ++use) {
+      if (!dwait(&s.slot_full[b], use & 1u, err)) break;
+      const Desc ds = s.slot_desc[b];
+      if (ds.flags & kEnd) break;
+      const float4* red = s.u.red[b];
       const bool down = (ds.flags & kDown) != 0;
       // lane L holds the fragment (rows g, g+8) x (tokens 2c, 2c+1) of both tiles
       float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
-        const float4 a = red[w * 32 + lane], bq = red[(8 + w) * 32 + lane];
-        v0.x += a.x; v0.y += a.y; v0.z += a.z; v0.w += a.w;
-        v1.x += bq.x; v1.y += bq.y; v1.z += bq.z; v1.w += bq.w;
+        const float4 a = red[w * 32 + lane], q = red[(8 + w) * 32 + lane];
+        v0.x += a.x;
+        v0.y += a.y;
+        v0.z += a.z;
+        v0.w += a.w;
+        v1.x += q.x;
+        v1.y += q.y;
+        v1.z += q.z;
+        v1.w += q.w;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.slot_free[b]);  // partial sums consumed
       const float f0[4] = {v0.x, v0.y, v0.z, v0.w}, f1[4] = {v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -800,13 +842,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           yr[16 + row] = f1[q];
         }
       }
+      // each lane publishes its own h / y stores before the warp's release-add
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
       __syncwarp();
       int tile_last = 0;
       if (lane == 0) {
         if (!down) {
           asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.done1 + ds.cnt) : "memory");
         } else {
-          const int per_tile = (cnt.sh2 + s.meta[2]) / (d.H / kTile2);
+          if (routed_down < 0) routed_down = s.meta[2];
+          const int per_tile = (cnt.sh2 + routed_down) / (d.H / kTile2);
           int old;
           asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
                        : "=r"(old)
@@ -817,23 +862,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tile_last = __shfl_sync(0xffffffffu, tile_last, 0);
       if (tile_last) {
-        // last down task of this channel tile: combine it for every token
-        __threadfence();
+        // this task completed a channel tile: combine it for every token
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
         const int n0 = ds.tile * kTile2;
         for (int i = lane; i < d.T * kTile2; i += 32) {
           const int tok = i / kTile2, n = n0 + (i - tok * kTile2);
           float a = d.Is > 0 ? __ldcg(p.y + (size_t)(d.T * d.k + tok) * d.H + n) : 0.f;
-          for (int j = 0; j < d.k; ++j) {
-            const float w = __ldcg(p.r.wts + tok * d.k + j);
-            const int row = __ldcg(p.r.inv + tok * d.k + j);
-            a = fmaf(w, __ldcg(p.y + (size_t)row * d.H + n), a);
-          }
+          for (int j = 0; j < d.k; ++j)
+            a = fmaf(s.wts_s[tok * d.k + j], __ldcg(p.y + (size_t)s.inv_s[tok * d.k + j] * d.H + n), a);
           p.out[(size_t)tok * d.H + n] = f32_to_bf16_bits(a);
         }
         if (lane == 0) p.tile_cnt[ds.tile] = 0;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.red_free[bsel]);
     }
   }
 
@@ -848,10 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __threadfence();
     for (int i = threadIdx.x; i < (d.E + 1) * kMaxPass; i += blockDim.x) p.done1[i] = 0;
     for (int i = threadIdx.x; i < d.H / kTile2; i += blockDim.x) p.tile_cnt[i] = 0;
-    if (threadIdx.x == 0) {
-      p.sync[0] = 0u;
-      p.sync[1] = 0u;
-    }
+    if (threadIdx.x == 0) p.sync[0] = 0u;
     __syncthreads();
     if (threadIdx.x == 0) {
       __threadfence();
@@ -861,8 +898,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace
-
-int decode_smem_bytes() { return (int)sizeof(Smem); }
 
 cudaError_t decode_setup(int* ctas_per_sm) {
   cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
