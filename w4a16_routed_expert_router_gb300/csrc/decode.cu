@@ -17,15 +17,17 @@
 // one expert over all of K, for one pass of <= 8 rows of that expert.
 //
 // Warp roles (one CTA per SM):
-//  * 16 consumer warps. First the router: every CTA scores one or two experts
-//    for all tokens (fp32), publishes the logits, waits until every CTA has
-//    (a counter), then computes the whole routing itself in shared memory
-//    (top-k, histogram, scan, stable permutation, task lists). Computing it
-//    redundantly per CTA keeps the critical path at two global round trips.
-//    Then the consumers stream stages: warp w takes K-group (w % 8) of tile
-//    (w / 8); exact INT4 -> bf16 in registers, mma.sync m16n8k16 with weights
-//    as A and up to 8 rows as B, group scales applied in fp32. At the end of
-//    a task each warp drops its partial sums into a slot and moves on.
+//  * 4 router warps: every CTA scores one or two experts for all tokens
+//    (fp32), publishes the logits, waits until every CTA has (a counter),
+//    then computes the whole routing itself in shared memory (top-k,
+//    histogram, scan, stable permutation, task lists). Computing it
+//    redundantly per CTA keeps the critical path at two global round trips,
+//    and it overlaps the shared expert's work, which needs no routing.
+//  * 16 consumer warps stream stages from the start: warp w takes K-group
+//    (w % 8) of tile (w / 8); exact INT4 -> bf16 in registers, mma.sync
+//    m16n8k16 with weights as A and up to 8 rows as B, group scales applied
+//    in fp32. At the end of a task each warp drops its partial sums into a
+//    slot and moves on.
 //  * 1 producer warp: decodes tasks and fills a 5-stage ring (2-D TMA boxes
 //    of 16 rows x 512 B per tile, scale boxes, bulk copies of the activation
 //    rows) with a descriptor per stage. Down tasks need the h rows of their
@@ -52,8 +54,11 @@ namespace {
 
 constexpr int kCW = 16;                      // consumer warps
 constexpr int kEW = 4;                       // epilogue warps (= slots)
+constexpr int kRW = 4;                       // router warps
 constexpr int kProd = kCW;                   // producer warp index
-constexpr int kThreads = (kCW + 1 + kEW) * 32;
+constexpr int kEpi0 = kCW + 1;               // first epilogue warp
+constexpr int kRtr0 = kEpi0 + kEW;           // first router warp
+constexpr int kThreads = (kCW + 1 + kEW + kRW) * 32;
 constexpr int kR = 8;                        // rows per pass (MMA N)
 constexpr int kS = 5;                        // ring stages
 constexpr int kWB = 2 * 16 * 512;            // 2 tiles x 16 rows x 512 B (8 K-groups)
@@ -72,10 +77,9 @@ struct Desc {
 
 struct Smem {
   uint8_t stage[kS][kStageB];
-  union {
-    float4 red[kEW][kCW * 32];          // task-end partial sums, one slot per epilogue warp
-    float part[2][kCW][kSmallT];        // router: per-warp partial logits of 2 experts
-  } u;
+  float4 red[kEW][kCW * 32];            // task-end partial sums, one slot per epilogue warp
+  float part[2][kRW][kSmallT];          // router: per-warp partial logits of 2 experts
+  float bias_s[kMaxExperts];
   Desc slot_desc[kEW];
   Desc desc[kS];
   int ids_s[kItems];
@@ -87,7 +91,7 @@ struct Smem {
   int pre1[kMaxExperts + 2];
   int pre2[kMaxExperts + 2];
   int offsets[kMaxExperts + 2];
-  int4 scan[kCW];
+  int4 scan[kRW];
   int meta[4];                          // n_act, routed gate/up tasks, routed down tasks
   uint64_t full[kS];
   uint64_t empty[kS];
@@ -124,8 +128,8 @@ struct Task {
 
 __device__ __forceinline__ int passes_of(int rows) { return (rows + kR - 1) / kR; }
 
-// named barrier of the 512 consumer threads
-__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+// named barrier of the router warps
+__device__ __forceinline__ void rbar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __device__ __forceinline__ bool aborted(const unsigned* err) {
   return (*reinterpret_cast<const volatile unsigned*>(err) & kErrTimeout) != 0;
@@ -294,7 +298,7 @@ __device__ __forceinline__ void warp_topk(const float* logit_row, const float* b
     if (e < E) {
       const float s = 1.0f / (1.0f + expf(-sc[i]));
       sc[i] = s;
-      sel[i] = s + __ldg(bias + e);
+      sel[i] = s + bias[e];
     } else {
       sel[i] = -INFINITY;
     }
@@ -340,9 +344,9 @@ __device__ __forceinline__ void warp_topk(const float* logit_row, const float* b
   *out_w = chosen_s / sum;
 }
 
-// Exclusive scan of four ints over the 512 consumer threads.
-__device__ __forceinline__ int4 cscan4(int4 v, int4* scr, int4* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Exclusive scan of four ints over the 128 router threads (t = router thread).
+__device__ __forceinline__ int4 rscan4(int4 v, int t, int4* scr, int4* total) {
+  const int lane = t & 31, warp = t >> 5;
   int4 inc = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -356,9 +360,9 @@ __device__ __forceinline__ int4 cscan4(int4 v, int4* scr, int4* total) {
     }
   }
   if (lane == 31) scr[warp] = inc;
-  cbar();
+  rbar();
   int4 base = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
-  for (int w = 0; w < kCW; ++w) {
+  for (int w = 0; w < kRW; ++w) {
     const int4 s = scr[w];
     if (w < warp) {
       base.x += s.x;
@@ -371,18 +375,19 @@ __device__ __forceinline__ int4 cscan4(int4 v, int4* scr, int4* total) {
     tot.z += s.z;
     tot.w += s.w;
   }
-  cbar();
+  rbar();
   *total = tot;
   return make_int4(base.x + inc.x - v.x, base.y + inc.y - v.y, base.z + inc.z - v.z,
                    base.w + inc.w - v.w);
 }
 
-// Consumer warps: score this CTA's experts, wait for every CTA's logits, then
+// Router warps: score this CTA's experts, wait for every CTA's logits, then
 // compute the whole routing in shared memory. Returns false on timeout.
 __device__ bool router_phase(Smem& s, const DecodeParams& p) {
   const Dims& d = p.d;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int kw = d.H / kCW;  // K slice of one warp
+  const int tid = threadIdx.x - kRtr0 * 32, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < d.E; e += kRW * 32) s.bias_s[e] = __ldg(p.router_bias + e);
+  const int kw = d.H / kRW;  // K slice of one warp
   const int nf = kw / 4;
   for (int eb = blockIdx.x; eb < d.E; eb += 2 * gridDim.x) {
     const int e0 = eb, e1 = eb + gridDim.x;
@@ -393,11 +398,11 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
     for (int t = 0; t < d.T; ++t) {
       const uint2* xr = reinterpret_cast<const uint2*>(p.x + (size_t)t * d.H + warp * kw);
       float a0 = 0.f, a1 = 0.f;
-      for (int f0 = 0; f0 < nf; f0 += 64) {
-        float4 v0[2], v1[2];
-        uint2 xv[2];
+      for (int f0 = 0; f0 < nf; f0 += 128) {
+        float4 v0[4], v1[4];
+        uint2 xv[4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < 4; ++u) {
           const int f = f0 + u * 32 + lane;
           const bool ok = f < nf;
           v0[u] = ok ? __ldg(w0 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -405,7 +410,7 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
           xv[u] = ok ? __ldg(xr + f) : make_uint2(0u, 0u);
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < 4; ++u) {
           const float x0 = __uint_as_float(xv[u].x << 16), x1 = __uint_as_float(xv[u].x & 0xffff0000u);
           const float x2 = __uint_as_float(xv[u].y << 16), x3 = __uint_as_float(xv[u].y & 0xffff0000u);
           a0 = fmaf(x0, v0[u].x, a0);
@@ -424,20 +429,20 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
         a1 += __shfl_xor_sync(0xffffffffu, a1, o);
       }
       if (lane == 0) {
-        s.u.part[0][warp][t] = a0;
-        s.u.part[1][warp][t] = a1;
+        s.part[0][warp][t] = a0;
+        s.part[1][warp][t] = a1;
       }
     }
-    cbar();
+    rbar();
     if (tid < 2 * d.T) {
       const int slot = tid / d.T, t = tid - slot * d.T;
       if (slot == 0 || has1) {
         float v = 0.f;
-        for (int w = 0; w < kCW; ++w) v += s.u.part[slot][w][t];
+        for (int w = 0; w < kRW; ++w) v += s.part[slot][w][t];
         p.r.logits[(size_t)t * d.E + (slot ? e1 : e0)] = v;
       }
     }
-    cbar();
+    rbar();
   }
   // publish this CTA's logits and wait for everybody's
   if (tid == 0) {
@@ -445,16 +450,16 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
     atomicAdd(&p.sync[0], 1u);
     s.flag = wait_counter(reinterpret_cast<const int*>(p.sync), (int)gridDim.x, p.r.err) ? 1 : 0;
   }
-  if (tid < kMaxExperts) s.counts_s[tid] = 0;
-  cbar();
+  for (int e = tid; e < kMaxExperts; e += kRW * 32) s.counts_s[e] = 0;
+  rbar();
   if (!s.flag) return false;
   (void)ld_acquire(reinterpret_cast<const int*>(p.sync));
 
   // ---- the routing of every token, in shared memory
-  for (int t = warp; t < d.T; t += kCW) {
+  for (int t = warp; t < d.T; t += kRW) {
     int id;
     float w;
-    warp_topk(p.r.logits + (size_t)t * d.E, p.router_bias, d.E, d.k, lane, &id, &w);
+    warp_topk(p.r.logits + (size_t)t * d.E, s.bias_s, d.E, d.k, lane, &id, &w);
     if (lane < d.k) {
       if (id < 0 || id >= d.E) {
         atomicOr(p.r.err, kErrRange);
@@ -465,21 +470,38 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
       atomicAdd(&s.counts_s[id], 1);
     }
   }
-  cbar();
+  rbar();
   {
-    const int e = tid;
-    const int c = (e < d.E) ? s.counts_s[e] : 0;
-    const int ps = passes_of(c);
-    const int4 v = make_int4(c, c > 0 ? 1 : 0, ps * (d.I / kTile1), ps * (d.H / kTile2));
+    // two experts per thread: e = 2 tid, 2 tid + 1
+    int c2[2], ps[2];
+    int4 v = make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int e = 2 * tid + i;
+      c2[i] = (e < d.E) ? s.counts_s[e] : 0;
+      ps[i] = passes_of(c2[i]);
+      v.x += c2[i];
+      v.y += c2[i] > 0 ? 1 : 0;
+      v.z += ps[i] * (d.I / kTile1);
+      v.w += ps[i] * (d.H / kTile2);
+    }
     int4 tot;
-    const int4 ex = cscan4(v, s.scan, &tot);
-    if (e < d.E) {
-      s.offsets[e] = ex.x;
-      if (c > 0) {
-        s.active[ex.y] = e;
-        s.pre1[ex.y] = ex.z;
-        s.pre2[ex.y] = ex.w;
+    int4 ex = rscan4(v, tid, s.scan, &tot);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int e = 2 * tid + i;
+      if (e < d.E) {
+        s.offsets[e] = ex.x;
+        if (c2[i] > 0) {
+          s.active[ex.y] = e;
+          s.pre1[ex.y] = ex.z;
+          s.pre2[ex.y] = ex.w;
+        }
       }
+      ex.x += c2[i];
+      ex.y += c2[i] > 0 ? 1 : 0;
+      ex.z += ps[i] * (d.I / kTile1);
+      ex.w += ps[i] * (d.H / kTile2);
     }
     if (tid == 0) {
       s.offsets[d.E] = tot.x;
@@ -490,9 +512,9 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
       s.meta[2] = tot.w;
     }
   }
-  cbar();
+  rbar();
   const int n = d.T * d.k;
-  for (int i = tid; i < n; i += kCW * 32) {
+  for (int i = tid; i < n; i += kRW * 32) {
     const int ei = s.ids_s[i];
     int rank = 0;
     for (int j = 0; j < i; ++j) rank += (s.ids_s[j] == ei);
@@ -500,21 +522,21 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
     s.perm_s[pos] = i / d.k;
     s.inv_s[i] = pos;
   }
-  cbar();
+  rbar();
   if (tid == 0) mbar_arrive(&s.route_ready);
   // one CTA also writes the routing out (the get-routing hook reads it)
   if (blockIdx.x == 0) {
-    for (int i = tid; i < n; i += kCW * 32) {
+    for (int i = tid; i < n; i += kRW * 32) {
       p.r.ids[i] = s.ids_s[i];
       p.r.wts[i] = s.wts_s[i];
       p.r.perm[i] = s.perm_s[i];
       p.r.inv[i] = s.inv_s[i];
     }
-    for (int e = tid; e <= d.E; e += kCW * 32) {
+    for (int e = tid; e <= d.E; e += kRW * 32) {
       p.r.offsets[e] = s.offsets[e];
       if (e < d.E) p.r.counts[e] = s.counts_s[e];
     }
-    for (int a = tid; a <= s.meta[0]; a += kCW * 32) {
+    for (int a = tid; a <= s.meta[0]; a += kRW * 32) {
       if (a < s.meta[0]) p.r.active[a] = s.active[a];
       p.r.task1[a] = s.pre1[a];
       p.r.task2[a] = s.pre2[a];
@@ -707,7 +729,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kCW) {
     // ---------------------------------------------------------------- consumers
-    const bool routed = router_phase(s, p);
     const int g = lane >> 2, c = lane & 3;
     const int gw = warp & 7, tl = warp >> 3;
     const uint32_t stage0 = smem_u32(s.stage[0]);
@@ -718,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     int tseq = 0;  // tasks finished (the same sequence for all consumer warps)
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (; routed;) {
+    for (;;) {
       if (!dwait(&s.full[stage], phase, err)) break;
       const Desc ds = s.desc[stage];
       if (ds.flags & kEnd) break;
@@ -784,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = tseq % kEW;
       const uint32_t use = (uint32_t)(tseq / kEW);
       if (!dwait(&s.slot_free[b], (use & 1u) ^ 1u, err)) break;
-      s.u.red[b][warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      s.red[b][warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       if (warp == 0 && lane == 0) s.slot_desc[b] = ds;
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.slot_full[b]);
@@ -799,16 +820,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.slot_full[b]);
     }
+  } else if (warp >= kRtr0) {
+    // ---------------------------------------------------------------- router
+    router_phase(s, p);
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int b = warp - kCW - 1;  // this warp's slot
+    const int b = warp - kEpi0;  // this warp's slot
     const int g = lane >> 2, c = lane & 3;
     int routed_down = -1;
     for (uint32_t use = 0;; ++use) {
       if (!dwait(&s.slot_full[b], use & 1u, err)) break;
       const Desc ds = s.slot_desc[b];
       if (ds.flags & kEnd) break;
-      const float4* red = s.u.red[b];
+      const float4* red = s.red[b];
       const bool down = (ds.flags & kDown) != 0;
       // lane L holds the fragment (rows g, g+8) x (tokens 2c, 2c+1) of both tiles
       float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
@@ -850,7 +874,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!down) {
           asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.done1 + ds.cnt) : "memory");
         } else {
-          if (routed_down < 0) routed_down = s.meta[2];
+          if (routed_down < 0) {
+            // a shared-expert down task can finish before the routing exists
+            routed_down = dwait(&s.route_ready, 0, err) ? s.meta[2] : 0;
+          }
           const int per_tile = (cnt.sh2 + routed_down) / (d.H / kTile2);
           int old;
           asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
