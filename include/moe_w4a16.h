@@ -148,6 +148,31 @@ int moe_w4a16_check_device_errors(moe_w4a16_handle* h, uint32_t* flags);
 int moe_w4a16_last_launches(moe_w4a16_handle* h, int32_t* count, const char** names,
                             float* ms, int32_t capacity);
 
+/* Forward without any device allocation (no handle, no workspace).
+ *
+ * Not a step of the layer itself: the pages have no counterpart. It exists
+ * for callers that cannot call cudaMalloc -- code running while a stream is
+ * captured into a CUDA graph, plugins confined to a memory budget owned by a
+ * host framework, latency-critical paths that cannot afford the allocator.
+ * Scratch is a fixed 6 MiB array declared by the library as a __device__
+ * variable; every GPU that loads the library holds it until the process
+ * exits. Limits: num_tokens <= MOE_W4A16_NOALLOC_MAX_TOKENS, and the layer's
+ * scratch (routing, h, y, counters) must fit the array; larger requests
+ * return MOE_W4A16_ERR_TOO_MANY_TOKENS or MOE_W4A16_ERR_UNSUPPORTED_SHAPE
+ * without launching anything.
+ *
+ * The first call on a device does a one-time set-up there (it resolves the
+ * array's device address and configures the kernel); make that first call
+ * before any stream capture. Every call uses the same array and leaves its
+ * contents behind, so calls that overlap on the GPU (other streams, other
+ * host threads) race with each other; the call clears the counters it needs
+ * at zero on `stream` itself. cfg->max_tokens and cfg->flags are ignored;
+ * x, out and the weights are device pointers as for moe_w4a16_forward.
+ * Device-side error flags are not reported by this entry point. */
+#define MOE_W4A16_NOALLOC_MAX_TOKENS 16
+int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint16_t* x, int32_t num_tokens,
+                              const moe_w4a16_weights* w, uint16_t* out, void* stream);
+
 /* Static description of a status code. */
 const char* moe_w4a16_status_string(int status);
 

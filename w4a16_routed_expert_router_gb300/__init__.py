@@ -37,7 +37,9 @@ EXPORTS = (
     "moe_w4a16_check_device_errors",
     "moe_w4a16_last_launches",
     "moe_w4a16_status_string",
+    "moe_w4a16_forward_noalloc",
 )
+MOE_W4A16_NOALLOC_MAX_TOKENS = 16
 
 
 class MoeError(RuntimeError):
@@ -91,6 +93,7 @@ def lib() -> ctypes.CDLL:
             "moe_w4a16_last_launches": ([vp, ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_char_p),
                                          ctypes.POINTER(ctypes.c_float), i32], ctypes.c_int),
             "moe_w4a16_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "moe_w4a16_forward_noalloc": ([cfgp, vp, i32, wp, vp, vp], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -142,6 +145,14 @@ def moe_w4a16_forward_host(handle, x_host_ptr: int, num_tokens: int,
                            weights: moe_w4a16_weights, out_host_ptr: int, stream: int = 0) -> None:
     _check(lib().moe_w4a16_forward_host(handle, x_host_ptr, num_tokens, ctypes.byref(weights),
                                         out_host_ptr, stream), "moe_w4a16_forward_host")
+
+
+def moe_w4a16_forward_noalloc(cfg: moe_w4a16_config, x_ptr: int, num_tokens: int,
+                              weights: moe_w4a16_weights, out_ptr: int, stream: int = 0) -> None:
+    """Forward on the library's fixed scratch array: no handle, no allocation."""
+    _check(lib().moe_w4a16_forward_noalloc(ctypes.byref(cfg), x_ptr, num_tokens,
+                                           ctypes.byref(weights), out_ptr, stream),
+           "moe_w4a16_forward_noalloc")
 
 
 def moe_w4a16_get_routing(handle, ids=0, wts=0, offsets=0, perm=0, inv=0, stream=0) -> None:

@@ -3,6 +3,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "../../include/moe_w4a16.h"
@@ -518,3 +519,185 @@ int moe_w4a16_last_launches(moe_w4a16_handle* h, int32_t* count, const char** na
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------
+// Forward without device allocation.
+//
+// Some callers cannot call cudaMalloc: code that runs while a stream is being
+// captured into a CUDA graph (allocation is not allowed there), plugins that
+// must live inside a memory budget owned by a host framework, and latency-
+// critical paths that cannot afford the allocator's synchronisation. For them
+// the decode-sized forward runs on a fixed scratch array that the library
+// declares itself: every GPU that loads the library holds it until exit.
+// ------------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(6) << 20;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+  bool ready = false;
+  unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch
+  int grid = 0;
+};
+constexpr int kMaxDevices = 64;
+NoAllocDevice g_noalloc[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+struct NoAllocLayout {
+  size_t off[16];
+  size_t total;
+};
+
+NoAllocLayout noalloc_plan(const moe_w4a16_config& c, int T) {
+  const size_t E = c.num_experts, k = c.top_k, H = c.hidden, Tz = T;
+  const size_t rows = Tz * k + Tz;
+  const size_t hstride = c.inter > c.shared_inter ? c.inter : c.shared_inter;
+  const size_t sizes[] = {
+      Tz * E * 4,                                        // 0 logits
+      Tz * k * 4,                                        // 1 ids
+      Tz * k * 4,                                        // 2 wts
+      E * 4,                                             // 3 counts
+      (E + 1) * 4,                                       // 4 offsets
+      (E + 1) * 4,                                       // 5 active
+      kMetaWords * 4,                                    // 6 meta
+      (E + 2) * 4,                                       // 7 task1
+      (E + 2) * 4,                                       // 8 task2
+      Tz * k * 4,                                        // 9 perm
+      Tz * k * 4,                                        // 10 inv
+      4,                                                 // 11 err
+      decode_counter_ints(c.num_experts, c.hidden) * 4,  // 12 counters
+      rows * hstride * 2,                                // 13 h
+      rows * H * 4,                                      // 14 y
+  };
+  NoAllocLayout L;
+  size_t o = 0;
+  for (size_t i = 0; i < sizeof(sizes) / sizeof(sizes[0]); ++i) {
+    L.off[i] = o;
+    o += align256(sizes[i]);
+  }
+  L.total = o;
+  return L;
+}
+
+}  // namespace
+
+extern "C" int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint16_t* x,
+                                         int32_t T, const moe_w4a16_weights* w, uint16_t* out,
+                                         void* stream) {
+  int st = validate_config(cfg);
+  if (st != MOE_W4A16_OK) return st;
+  const moe_w4a16_config& c = *cfg;
+  if (T < 0) return MOE_W4A16_ERR_INVALID_ARG;
+  if (T > MOE_W4A16_NOALLOC_MAX_TOKENS) return MOE_W4A16_ERR_TOO_MANY_TOKENS;
+  if ((st = validate_weights(c, w)) != MOE_W4A16_OK) return st;
+  if (T == 0) return MOE_W4A16_OK;
+  if (!x || !out) return MOE_W4A16_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out)) return MOE_W4A16_ERR_MISALIGNED;
+  {
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), oa = reinterpret_cast<uintptr_t>(out);
+    const uintptr_t n = (uintptr_t)T * c.hidden * 2;
+    if (xa < oa + n && oa < xa + n) return MOE_W4A16_ERR_INVALID_ARG;
+  }
+  const NoAllocLayout L = noalloc_plan(c, T);
+  if (L.total > kNoAllocScratchBytes) return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
+
+  int dev = -1;
+  if ((st = cuda_status(cudaGetDevice(&dev))) != MOE_W4A16_OK) return st;
+  if (dev < 0 || dev >= kMaxDevices) return MOE_W4A16_ERR_NO_DEVICE;
+  NoAllocDevice nd;
+  {
+    // one-time set-up per device, with that device current: resolve the
+    // device address of the scratch array (the host-side symbol is only a
+    // stand-in) and configure the decode kernel
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoAllocDevice& gd = g_noalloc[dev];
+    if (!gd.ready) {
+      cudaDeviceProp prop;
+      if ((st = cuda_status(cudaGetDeviceProperties(&prop, dev))) != MOE_W4A16_OK) return st;
+      if (prop.major != 10 || prop.minor != 3) return MOE_W4A16_ERR_NO_DEVICE;
+      void* ptr = nullptr;
+      if ((st = cuda_status(cudaGetSymbolAddress(&ptr, g_noalloc_scratch))) != MOE_W4A16_OK)
+        return st;
+      int per_sm = 0;
+      if ((st = cuda_status(decode_setup(&per_sm))) != MOE_W4A16_OK) return st;
+      if (per_sm < 1) return MOE_W4A16_ERR_CUDA;
+      gd.scratch = static_cast<unsigned char*>(ptr);
+      gd.grid = prop.multiProcessorCount * per_sm;
+      gd.ready = true;
+    }
+    nd = gd;
+  }
+
+  unsigned char* b = nd.scratch;
+  Routing r;
+  r.logits = reinterpret_cast<float*>(b + L.off[0]);
+  r.ids = reinterpret_cast<int*>(b + L.off[1]);
+  r.wts = reinterpret_cast<float*>(b + L.off[2]);
+  r.counts = reinterpret_cast<int*>(b + L.off[3]);
+  r.offsets = reinterpret_cast<int*>(b + L.off[4]);
+  r.active = reinterpret_cast<int*>(b + L.off[5]);
+  r.meta = reinterpret_cast<int*>(b + L.off[6]);
+  r.task1 = reinterpret_cast<int*>(b + L.off[7]);
+  r.task2 = reinterpret_cast<int*>(b + L.off[8]);
+  r.perm = reinterpret_cast<int*>(b + L.off[9]);
+  r.inv = reinterpret_cast<int*>(b + L.off[10]);
+  r.blockcnt = nullptr;
+  r.blockbase = nullptr;
+  r.tickets = nullptr;
+  r.err = reinterpret_cast<unsigned*>(b + L.off[11]);
+  int* counters = reinterpret_cast<int*>(b + L.off[12]);
+  uint16_t* hbuf = reinterpret_cast<uint16_t*>(b + L.off[13]);
+  float* ybuf = reinterpret_cast<float*>(b + L.off[14]);
+  const int hstride = c.inter > c.shared_inter ? c.inter : c.shared_inter;
+
+  // tensor maps, encoded on the host for this call
+  const bool has_sh = c.shared_inter > 0;
+  const bool scale_tma = (c.hidden / kGroup) % 8 == 0 && (c.inter / kGroup) % 8 == 0 &&
+                         (!has_sh || (c.shared_inter / kGroup) % 8 == 0);
+  const long long r13 = (long long)c.num_experts * 2 * c.inter, r2 = (long long)c.num_experts * c.hidden;
+  DecodeWeights dw;
+  dw.router_w = w->router_w;
+  dw.router_bias = w->router_bias;
+  dw.s13_routed = w->w13_s;
+  dw.s13_shared = has_sh ? w->sh_w13_s : w->w13_s;
+  dw.s2_routed = w->w2_s;
+  dw.s2_shared = has_sh ? w->sh_w2_s : w->w2_s;
+  dw.scale_tma = scale_tma;
+  if ((st = encode_int4_map2d(&dw.tm13r, w->w13_q, r13, c.hidden)) != MOE_W4A16_OK) return st;
+  if ((st = encode_int4_map2d(&dw.tm2r, w->w2_q, r2, c.inter)) != MOE_W4A16_OK) return st;
+  dw.tm13s = dw.tm13r;
+  dw.tm2s = dw.tm2r;
+  if (has_sh) {
+    if ((st = encode_int4_map2d(&dw.tm13s, w->sh_w13_q, 2LL * c.shared_inter, c.hidden)) != MOE_W4A16_OK)
+      return st;
+    if ((st = encode_int4_map2d(&dw.tm2s, w->sh_w2_q, c.hidden, c.shared_inter)) != MOE_W4A16_OK)
+      return st;
+  }
+  dw.ts13r = dw.tm13r;
+  dw.ts2r = dw.tm2r;
+  if (scale_tma) {
+    if ((st = encode_scale_map(&dw.ts13r, w->w13_s, r13, c.hidden)) != MOE_W4A16_OK) return st;
+    if ((st = encode_scale_map(&dw.ts2r, w->w2_s, r2, c.inter)) != MOE_W4A16_OK) return st;
+  }
+  dw.ts13s = dw.ts13r;
+  dw.ts2s = dw.ts2r;
+  if (scale_tma && has_sh) {
+    if ((st = encode_scale_map(&dw.ts13s, w->sh_w13_s, 2LL * c.shared_inter, c.hidden)) != MOE_W4A16_OK)
+      return st;
+    if ((st = encode_scale_map(&dw.ts2s, w->sh_w2_s, c.hidden, c.shared_inter)) != MOE_W4A16_OK)
+      return st;
+  }
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: clear the counters and
+  // the error word this call relies on starting at zero
+  if ((st = cuda_status(cudaMemsetAsync(counters, 0,
+                                        decode_counter_ints(c.num_experts, c.hidden) * 4, s))) !=
+      MOE_W4A16_OK)
+    return st;
+  if ((st = cuda_status(cudaMemsetAsync(r.err, 0, 4, s))) != MOE_W4A16_OK) return st;
+  Dims d{T, c.hidden, c.num_experts, c.top_k, c.inter, c.shared_inter};
+  LaunchLog log;
+  return cuda_status(launch_decode(d, r, dw, x, hbuf, hstride, ybuf, out, counters, nd.grid, s, log));
+}
