@@ -70,8 +70,11 @@ enum moe_w4a16_status {
 };
 
 /* config.flags */
-#define MOE_W4A16_FLAG_FORCE_GEMV 0x1u   /* always use the split-K GEMV experts   */
-#define MOE_W4A16_FLAG_FORCE_TC 0x2u     /* always use the tensor-core experts    */
+/* Expert paths: up to 64 tokens, one fused split-K GEMV kernel; above that,
+ * tcgen05 tensor-core GEMMs when hidden % 256 == 0, else split-K GEMVs. */
+#define MOE_W4A16_FLAG_FORCE_GEMV 0x1u   /* > 64 tokens: split-K GEMV experts     */
+#define MOE_W4A16_FLAG_FORCE_TC 0x2u     /* tensor-core experts at every size     */
+                                         /* (create fails if hidden % 256 != 0)   */
 #define MOE_W4A16_FLAG_PROFILE 0x4u      /* time each kernel with CUDA events     */
 
 /* device error flag bits (moe_w4a16_check_device_errors) */

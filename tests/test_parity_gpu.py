@@ -61,6 +61,52 @@ def test_tiny_layer_parity(tiny, T):
     obj.close()
 
 
+@pytest.mark.parametrize("flags,T", [
+    (moe.MOE_W4A16_FLAG_FORCE_TC, 1), (moe.MOE_W4A16_FLAG_FORCE_TC, 16),
+    (moe.MOE_W4A16_FLAG_FORCE_TC, 64), (moe.MOE_W4A16_FLAG_FORCE_TC, 300),
+    (moe.MOE_W4A16_FLAG_FORCE_GEMV, 65), (moe.MOE_W4A16_FLAG_FORCE_GEMV, 200)])
+def test_tiny_layer_parity_forced_path(tiny, flags, T):
+    shape, tensors = tiny
+    layer = mc.layer_with_tokens(shape, T)
+    ref = mc.oracle(layer)
+    obj = _layer_obj(layer, tensors, max_tokens=512, flags=flags)
+    out, rt = _run(obj, layer.x)
+    mc.check_routing(rt, ref, shape.experts)
+    mc.check_output(out, ref["out"])
+    names = [n for n, _ in moe.moe_w4a16_last_launches(obj.handle)]
+    if flags == moe.MOE_W4A16_FLAG_FORCE_TC:
+        assert "tc_gate_up_swiglu" in names and "tc_down" in names
+    else:
+        assert "gemv_gate_up_swiglu" in names or "decode_fused" in names
+    obj.close()
+
+
+def test_tiny_default_path_above_64_tokens_is_tensor_core(tiny):
+    shape, tensors = tiny
+    layer = mc.layer_with_tokens(shape, 65)
+    obj = _layer_obj(layer, tensors, 128)
+    _run(obj, layer.x)
+    names = [n for n, _ in moe.moe_w4a16_last_launches(obj.handle)]
+    assert names[-3:] == ["tc_gate_up_swiglu", "tc_down", "combine"]
+    obj.close()
+
+
+def test_tiny_hot_expert_spans_several_row_tiles(tiny):
+    # 600 rows of one expert: three 256-row tiles, the last one ragged (88 rows)
+    shape, tensors = tiny
+    bias = np.zeros(shape.experts, np.float32)
+    bias[5] = 4.0
+    layer = mc.layer_with_tokens(shape, 600, bias=bias)
+    ref = mc.oracle(layer)
+    assert (ref["ids"][:, 0] == 5).all()
+    obj = _layer_obj(layer, tensors, 600, bias=bias)
+    out, rt = _run(obj, layer.x)
+    assert rt["offsets"][6] - rt["offsets"][5] == 600
+    mc.check_routing(rt, ref, shape.experts)
+    mc.check_output(out, ref["out"])
+    obj.close()
+
+
 def test_tiny_one_expert_takes_every_token(tiny):
     shape, tensors = tiny
     bias = np.zeros(shape.experts, np.float32)
@@ -170,6 +216,21 @@ def test_zipf2048_routing_and_sampled_outputs(full):
     rt, _ = _full_case(full, "zipf2048", sample)
     counts = np.diff(rt["offsets"])
     assert counts.max() >= 1800 and (counts < 10).sum() >= 60
+
+
+def test_zipf2048_gemv_path_sampled_outputs(full):
+    shape = ms.CONFIGS["zipf2048"]
+    layer = mc.layer_with_tokens(shape)
+    subset = np.array([0, 777, 2047])
+    ref = mc.oracle(layer, subset=subset)
+    obj = _layer_obj(layer, full, shape.tokens, flags=moe.MOE_W4A16_FLAG_FORCE_GEMV,
+                     bias=layer.router_b)
+    out, rt = _run(obj, layer.x)
+    mc.check_routing(rt, ref, shape.experts)
+    mc.check_output(out[subset], ref["out"])
+    names = [n for n, _ in moe.moe_w4a16_last_launches(obj.handle)]
+    assert "gemv_down" in names
+    obj.close()
 
 
 def test_prefill8192_routing_and_sampled_outputs(full):

@@ -38,13 +38,28 @@ struct Routing {
   int* meta;          // [kMetaWords]: see Meta*
   int* task1;         // [E + 2] prefix of gate/up GEMV tasks per active expert
   int* task2;         // [E + 2] prefix of down GEMV tasks per active expert
+  int* task3;         // [E + 2] prefix of gate/up tensor-core tasks per active expert
+  int* task4;         // [E + 2] prefix of down tensor-core tasks per active expert
+  uint16_t* xperm;    // [T*k + T, H] x rows in expert order (+ shared rows), interleaved
   int* blockcnt;      // [nblk, E] per-CTA expert counts (large-T routing)
   int* blockbase;     // [nblk, E] first row of each CTA's items per expert
   unsigned* tickets;  // [kTickets] last-block-done counters (self-resetting)
   unsigned* err;      // device error flag bits
 };
 
-enum Meta { kMetaActive = 0, kMetaTasks1 = 1, kMetaTasks2 = 2, kMetaWords = 8 };
+enum Meta {
+  kMetaActive = 0,
+  kMetaTasks1 = 1,
+  kMetaTasks2 = 2,
+  kMetaTc1 = 3,
+  kMetaTc2 = 4,
+  kMetaWords = 8
+};
+
+// Tensor-core expert path: an N-tile holds up to kTcN rows of one expert; a
+// gate/up task covers 128 gate + 128 up channels, a down task 2 x 128 output
+// channels.
+constexpr int kTcN = 256;
 enum Ticket { kTicketRouter = 0, kTicketTopk = 1, kTickets = 4 };
 
 // ------------------------------------------------------------------ PTX helpers

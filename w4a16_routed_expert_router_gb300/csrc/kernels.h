@@ -76,6 +76,27 @@ cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& 
                           uint16_t* h, int hstride, float* y, uint16_t* out, int* counters, int grid,
                           cudaStream_t s, LaunchLog& log);
 
+// Tensor-core (tcgen05) expert GEMMs for large batches.
+struct TcWeights {
+  const uint16_t* scale_routed;  // bf16 group scales (global loads when !scale_tma)
+  const uint16_t* scale_shared;
+  // 2-D views {K/8 words, rows} of the packed weights, box {8 words, 128 rows}
+  CUtensorMap wq_r, wq_s;
+  // 2-D views {K/128, rows} of the scales, box {K/128, 128} (when scale_tma)
+  CUtensorMap ws_r, ws_s;
+  int scale_tma;
+};
+cudaError_t tc_setup(int* ctas_per_sm);
+// gate/up + SwiGLU: xmap is a 2-D bf16 view {H, rows} of Routing::xperm with
+// box {64, 64} and 128-byte swizzle; writes h rows (interleaved order)
+cudaError_t launch_tc_gate_up(const Dims& d, const Routing& r, const TcWeights& w,
+                              const CUtensorMap& xmap, uint16_t* h, int hstride, int grid,
+                              cudaStream_t s, LaunchLog& log);
+// down: hmap is the same kind of view {hstride, rows} of h; writes y rows
+cudaError_t launch_tc_down(const Dims& d, const Routing& r, const TcWeights& w,
+                           const CUtensorMap& hmap, float* y, int grid, cudaStream_t s,
+                           LaunchLog& log);
+
 cudaError_t launch_combine(const Dims& d, const Routing& r, const float* y, uint16_t* out,
                            cudaStream_t s, LaunchLog& log);
 

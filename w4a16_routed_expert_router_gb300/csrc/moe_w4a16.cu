@@ -17,6 +17,8 @@ struct moe_w4a16_handle {
   int num_sms = 0;
   int gemv_grid = 0;
   int decode_grid = 0;
+  int tc_grid = 0;
+  bool tc_ok = false;           // shapes the tensor-core experts support
   int* counters = nullptr;      // decode kernel completion counters (self-resetting)
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -34,9 +36,13 @@ struct moe_w4a16_handle {
   // tensor-map cache keyed by the tensor pointers it was encoded for:
   // 0 w13_q, 1 w2_q, 2 sh_w13_q, 3 sh_w2_q (3-D, 1-group boxes), 4 w13_s, 5 w2_s,
   // 6 sh_w13_s, 7 sh_w2_s (scales), 8 w13_q, 9 w2_q, 10 sh_w13_q, 11 sh_w2_q
-  // (2-D, 8-group boxes)
-  const void* map_keys[12] = {};
-  CUtensorMap maps[12];
+  // (2-D, 8-group boxes), 12..15 the same weights in 128-row boxes and 16..19
+  // their scales in 128-row boxes (tensor-core experts)
+  static constexpr int kMaps = 20;
+  const void* map_keys[kMaps] = {};
+  CUtensorMap maps[kMaps];
+  // views of the workspace's activation operands for the tensor-core experts
+  CUtensorMap xmap, hmap;
 };
 
 namespace {
@@ -118,6 +124,9 @@ Layout plan(const moe_w4a16_config& c) {
       Tm * H * 2,            // 18 x_dev
       Tm * H * 2,            // 19 out_dev
       decode_counter_ints(c.num_experts, c.hidden) * 4,  // 20 decode counters
+      rows * H * 2,          // 21 xperm
+      (E + 2) * 4,           // 22 task3
+      (E + 2) * 4,           // 23 task4
   };
   Layout L;
   size_t o = 0;
@@ -193,11 +202,49 @@ int encode_int4_map2d(CUtensorMap* m, const void* base, long long rows, int K) {
   return MOE_W4A16_OK;
 }
 
+int encode_2d(CUtensorMap* m, CUtensorMapDataType type, int esize, const void* base,
+              long long cols, long long rows, int box0, int box1, CUtensorMapSwizzle swz,
+              CUtensorMapL2promotion l2, const char* what) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MOE_W4A16_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * esize};
+  cuuint32_t box[2] = {(cuuint32_t)box0, (cuuint32_t)box1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    fprintf(stderr, "moe_w4a16: cuTensorMapEncodeTiled (%s) failed (%d)\n", what, (int)r);
+    return MOE_W4A16_ERR_CUDA;
+  }
+  return MOE_W4A16_OK;
+}
+
+// Tensor-core operands. Packed INT4 [rows, K/8] uint32 in boxes of 8 words x
+// 128 rows (one 64-wide K block of a 128-channel tile); its scales [rows,
+// K/128] in boxes of all K/128 groups x 128 rows; a bf16 activation matrix
+// [rows, cols] in boxes of 64 x 64 with the 128-byte swizzle the tensor core
+// reads.
+int encode_int4_map_tc(CUtensorMap* m, const void* base, long long rows, int K) {
+  return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, base, K / 8, rows, 8, 128,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "int4 tiles");
+}
+int encode_scale_map_tc(CUtensorMap* m, const void* base, long long rows, int K) {
+  return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, K / kGroup, rows, K / kGroup, 128,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "scale tiles");
+}
+int encode_act_map_tc(CUtensorMap* m, const void* base, long long cols, long long rows) {
+  return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, 64, 64,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "activations");
+}
+
 int get_map(moe_w4a16_handle* h, int slot, const void* base, long long rows, int K) {
   if (h->map_keys[slot] == base && base) return MOE_W4A16_OK;
-  const int st = slot < 4   ? encode_int4_map(&h->maps[slot], base, rows, K)
-                 : slot < 8 ? encode_scale_map(&h->maps[slot], base, rows, K)
-                            : encode_int4_map2d(&h->maps[slot], base, rows, K);
+  const int st = slot < 4    ? encode_int4_map(&h->maps[slot], base, rows, K)
+                 : slot < 8  ? encode_scale_map(&h->maps[slot], base, rows, K)
+                 : slot < 12 ? encode_int4_map2d(&h->maps[slot], base, rows, K)
+                 : slot < 16 ? encode_int4_map_tc(&h->maps[slot], base, rows, K)
+                             : encode_scale_map_tc(&h->maps[slot], base, rows, K);
   if (st == MOE_W4A16_OK) h->map_keys[slot] = base;
   return st;
 }
@@ -278,6 +325,20 @@ int moe_w4a16_create(const moe_w4a16_config* cfg, int device, moe_w4a16_handle**
     return st != MOE_W4A16_OK ? st : MOE_W4A16_ERR_CUDA;
   }
   h->decode_grid = h->num_sms * dec_per_sm;
+  // tensor-core experts: down tiles are 256 output channels wide; the scale
+  // boxes hold every K group of a row (at most 256)
+  h->tc_ok = cfg->hidden % 256 == 0 && cfg->hidden / kGroup <= 256 && cfg->inter / kGroup <= 256 &&
+             cfg->shared_inter / kGroup <= 256;
+  if ((cfg->flags & MOE_W4A16_FLAG_FORCE_TC) && !h->tc_ok) {
+    delete h;
+    return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
+  }
+  int tc_per_sm = 0;
+  if ((st = cuda_status(tc_setup(&tc_per_sm))) != MOE_W4A16_OK || tc_per_sm < 1) {
+    delete h;
+    return st != MOE_W4A16_OK ? st : MOE_W4A16_ERR_CUDA;
+  }
+  h->tc_grid = h->num_sms * tc_per_sm;
 
   const Layout L = plan(*cfg);
   if ((st = cuda_status(cudaMalloc(&h->ws, L.total))) != MOE_W4A16_OK) {
@@ -310,6 +371,17 @@ int moe_w4a16_create(const moe_w4a16_config* cfg, int device, moe_w4a16_handle**
   h->x_dev = reinterpret_cast<uint16_t*>(b + L.off[18]);
   h->out_dev = reinterpret_cast<uint16_t*>(b + L.off[19]);
   h->counters = reinterpret_cast<int*>(b + L.off[20]);
+  r.xperm = reinterpret_cast<uint16_t*>(b + L.off[21]);
+  r.task3 = reinterpret_cast<int*>(b + L.off[22]);
+  r.task4 = reinterpret_cast<int*>(b + L.off[23]);
+  if (h->tc_ok) {
+    const long long rows = (long long)cfg->max_tokens * (cfg->top_k + 1);
+    if ((st = encode_act_map_tc(&h->xmap, r.xperm, cfg->hidden, rows)) != MOE_W4A16_OK ||
+        (st = encode_act_map_tc(&h->hmap, h->h, h->hstride, rows)) != MOE_W4A16_OK) {
+      moe_w4a16_destroy(h);
+      return st;
+    }
+  }
 
   if (cfg->flags & MOE_W4A16_FLAG_PROFILE) {
     for (int i = 0; i < 2 * LaunchLog::kMax; ++i) cudaEventCreate(&h->events[i]);
@@ -397,7 +469,7 @@ int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t T, const m
   g2.scale_tma = scale_tma;
 
   cudaError_t e;
-  if (T <= kSmallT) {
+  if (T <= kSmallT && !(c.flags & MOE_W4A16_FLAG_FORCE_TC)) {
     // decode sizes: the whole layer in one cooperative persistent kernel
     if ((st = get_map(h, 8, w->w13_q, r13, c.hidden)) != MOE_W4A16_OK) return st;
     if ((st = get_map(h, 9, w->w2_q, r2, c.inter)) != MOE_W4A16_OK) return st;
@@ -428,7 +500,55 @@ int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t T, const m
     h->last_T = T;
     return MOE_W4A16_OK;
   }
-  if ((e = launch_route(d, h->r, x, w->router_w, w->router_bias, s, h->log)) != cudaSuccess)
+  const bool use_tc = h->tc_ok && !(c.flags & MOE_W4A16_FLAG_FORCE_GEMV);
+  if (use_tc) {
+    // tensor-core experts: routing also gathers x into expert order
+    if ((st = get_map(h, 12, w->w13_q, r13, c.hidden)) != MOE_W4A16_OK) return st;
+    if ((st = get_map(h, 13, w->w2_q, r2, c.inter)) != MOE_W4A16_OK) return st;
+    if (has_sh) {
+      if ((st = get_map(h, 14, w->sh_w13_q, 2LL * c.shared_inter, c.hidden)) != MOE_W4A16_OK)
+        return st;
+      if ((st = get_map(h, 15, w->sh_w2_q, c.hidden, c.shared_inter)) != MOE_W4A16_OK) return st;
+    }
+    if (scale_tma) {
+      if ((st = get_map(h, 16, w->w13_s, r13, c.hidden)) != MOE_W4A16_OK) return st;
+      if ((st = get_map(h, 17, w->w2_s, r2, c.inter)) != MOE_W4A16_OK) return st;
+      if (has_sh) {
+        if ((st = get_map(h, 18, w->sh_w13_s, 2LL * c.shared_inter, c.hidden)) != MOE_W4A16_OK)
+          return st;
+        if ((st = get_map(h, 19, w->sh_w2_s, c.hidden, c.shared_inter)) != MOE_W4A16_OK) return st;
+      }
+    }
+    TcWeights t1, t2;
+    t1.wq_r = h->maps[12];
+    t1.wq_s = has_sh ? h->maps[14] : h->maps[12];
+    t1.ws_r = scale_tma ? h->maps[16] : h->maps[12];
+    t1.ws_s = scale_tma && has_sh ? h->maps[18] : t1.ws_r;
+    t1.scale_routed = w->w13_s;
+    t1.scale_shared = has_sh ? w->sh_w13_s : w->w13_s;
+    t1.scale_tma = scale_tma;
+    t2.wq_r = h->maps[13];
+    t2.wq_s = has_sh ? h->maps[15] : h->maps[13];
+    t2.ws_r = scale_tma ? h->maps[17] : h->maps[13];
+    t2.ws_s = scale_tma && has_sh ? h->maps[19] : t2.ws_r;
+    t2.scale_routed = w->w2_s;
+    t2.scale_shared = has_sh ? w->sh_w2_s : w->w2_s;
+    t2.scale_tma = scale_tma;
+    if ((e = launch_route(d, h->r, x, w->router_w, w->router_bias, s, h->log)) != cudaSuccess)
+      return cuda_status(e);
+    if ((e = launch_tc_gate_up(d, h->r, t1, h->xmap, h->h, h->hstride, h->tc_grid, s, h->log)) !=
+        cudaSuccess)
+      return cuda_status(e);
+    if ((e = launch_tc_down(d, h->r, t2, h->hmap, h->y, h->tc_grid, s, h->log)) != cudaSuccess)
+      return cuda_status(e);
+    if ((e = launch_combine(d, h->r, h->y, out, s, h->log)) != cudaSuccess) return cuda_status(e);
+    h->last_T = T;
+    return MOE_W4A16_OK;
+  }
+  Routing rg = h->r;  // the GEMV experts read x in token order
+  rg.xperm = nullptr;
+  rg.task3 = rg.task4 = nullptr;
+  if ((e = launch_route(d, rg, x, w->router_w, w->router_bias, s, h->log)) != cudaSuccess)
     return cuda_status(e);
   if ((e = launch_gemv_gate_up(d, h->r, g1, x, h->h, h->hstride, h->gemv_grid, s, h->log)) !=
       cudaSuccess)
@@ -645,6 +765,9 @@ extern "C" int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint
   r.blockcnt = nullptr;
   r.blockbase = nullptr;
   r.tickets = nullptr;
+  r.task3 = nullptr;
+  r.task4 = nullptr;
+  r.xperm = nullptr;
   r.err = reinterpret_cast<unsigned*>(b + L.off[11]);
   int* counters = reinterpret_cast<int*>(b + L.off[12]);
   uint16_t* hbuf = reinterpret_cast<uint16_t*>(b + L.off[13]);

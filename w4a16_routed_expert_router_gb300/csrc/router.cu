@@ -142,6 +142,12 @@ __device__ void finish_counts(const Dims& d, const int* counts_s, int* offs_s, c
   const int4 v = make_int4(c, c > 0 ? 1 : 0, p * (d.I / kTile1), p * (d.H / kTile2));
   int4 tot;
   const int4 ex = block_scan4_256(v, scratch, &tot);
+  // tensor-core tasks: N-tiles of kTcN rows x channel tiles
+  const int nt = (c + kTcN - 1) / kTcN;
+  const int4 v2 = make_int4(nt * (d.I / 128), nt * (d.H / 256), 0, 0);
+  __syncthreads();
+  int4 tot2;
+  const int4 ex2 = block_scan4_256(v2, scratch, &tot2);
   if (e < d.E) {
     offs_s[e] = ex.x;
     r.offsets[e] = ex.x;
@@ -150,6 +156,10 @@ __device__ void finish_counts(const Dims& d, const int* counts_s, int* offs_s, c
       r.active[ex.y] = e;
       r.task1[ex.y] = ex.z;
       r.task2[ex.y] = ex.w;
+      if (r.task3) {
+        r.task3[ex.y] = ex2.x;
+        r.task4[ex.y] = ex2.y;
+      }
     }
   }
   if (threadIdx.x == 0) {
@@ -159,6 +169,12 @@ __device__ void finish_counts(const Dims& d, const int* counts_s, int* offs_s, c
     r.meta[kMetaActive] = tot.y;
     r.meta[kMetaTasks1] = tot.z;
     r.meta[kMetaTasks2] = tot.w;
+    if (r.task3) {
+      r.task3[tot.y] = tot2.x;
+      r.task4[tot.y] = tot2.y;
+    }
+    r.meta[kMetaTc1] = tot2.x;
+    r.meta[kMetaTc2] = tot2.y;
   }
   __syncthreads();
 }
@@ -292,6 +308,14 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
   __shared__ float ws[32][64 + 4];
   const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  if (blockIdx.y == 0 && r.xperm) {
+    // the shared expert's rows of the tensor-core operand: x in the
+    // interleaved order, after the T*k routed rows
+    const int rows = min(64, d.T - t0);
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t0 * d.H);
+    uint4* dst = reinterpret_cast<uint4*>(r.xperm + (size_t)(d.T * d.k + t0) * d.H);
+    for (int i = threadIdx.x; i < rows * d.H / 8; i += blockDim.x) dst[i] = interleave8(src[i]);
+  }
 
   float acc[4][4] = {};
   for (int k0 = 0; k0 < d.H; k0 += 32) {
@@ -390,7 +414,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 // Stable placement of one CTA's items (tokens [t0, t0 + kTopkTokens), items in
 // (token, slot) order). Items are ranked chunk by chunk: within a warp by
 // __match_any_sync, across warps by a per-warp count table.
-__global__ void __launch_bounds__(256) route_place_kernel(Dims d, Routing r) {
+__global__ void __launch_bounds__(256) route_place_kernel(const uint16_t* __restrict__ x, Dims d,
+                                                          Routing r) {
   __shared__ int run[kMaxExperts];
   __shared__ int wcnt[8][kMaxExperts];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -431,12 +456,23 @@ __global__ void __launch_bounds__(256) route_place_kernel(Dims d, Routing r) {
     }
     __syncthreads();
   }
+  if (r.xperm) {
+    // routed rows of the tensor-core operand: x[t] at its expert-sorted row,
+    // in the interleaved order (one warp per row)
+    const int h8 = d.H / 8;
+    for (int i = i0 + warp; i < i1; i += 8) {
+      const int pos = r.inv[i], t = i / d.k;
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d.H);
+      uint4* dst = reinterpret_cast<uint4*>(r.xperm + (size_t)pos * d.H);
+      for (int c = lane; c < h8; c += 32) dst[c] = interleave8(__ldg(src + c));
+    }
+  }
 }
 
 // ------------------------------------------------------------------ launcher
 cudaError_t launch_route(const Dims& d, const Routing& r, const uint16_t* x, const float* router_w,
                          const float* bias, cudaStream_t s, LaunchLog& log) {
-  if (d.T <= kSmallT) {
+  if (d.T <= kSmallT && !r.xperm) {
     log.begin("route_small", s);
     route_small_kernel<<<(d.E + 1) / 2, 256, 0, s>>>(x, router_w, bias, d, r);
     log.end(s);
@@ -450,7 +486,7 @@ cudaError_t launch_route(const Dims& d, const Routing& r, const uint16_t* x, con
   router_topk_kernel<<<nblk, 256, 0, s>>>(bias, d, r);
   log.end(s);
   log.begin("route_place", s);
-  route_place_kernel<<<nblk, 256, 0, s>>>(d, r);
+  route_place_kernel<<<nblk, 256, 0, s>>>(x, d, r);
   log.end(s);
   return cudaGetLastError();
 }
