@@ -78,8 +78,11 @@ CONFIGS = {
     "decode64": MoeShape("decode64", 64, 4096, 256, 6, 2048, 2048, 1001, 1002),
     "prefill8192": MoeShape("prefill8192", 8192, 4096, 256, 6, 2048, 2048, 1001, 1003),
     "zipf2048": MoeShape("zipf2048", 2048, 4096, 256, 6, 2048, 2048, 1001, 1004, zipf_s=1.1),
+    # profiler-sized stand-in for prefill8192: the same expert shape and about
+    # the same rows per expert (1536 * 6 / 48 = 192), a sixth of the weights
+    "prefill1536e48": MoeShape("prefill1536e48", 1536, 4096, 48, 6, 2048, 2048, 1001, 1005),
 }
-CONFIG_ORDER = ["tiny16", "decode1", "decode64", "prefill8192", "zipf2048"]
+CONFIG_ORDER = ["tiny16", "decode1", "decode64", "prefill8192", "zipf2048", "prefill1536e48"]
 
 GOLDEN_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                           "tests", "golden")

@@ -45,8 +45,18 @@ struct GemvWeights {
   int scale_tma;           // K / 128 is a multiple of 8: scales ride in the TMA stage
 };
 
+// logits_ready: r.logits already holds this batch's logits (tensor-core router)
 cudaError_t launch_route(const Dims& d, const Routing& r, const uint16_t* x, const float* router_w,
-                         const float* bias, cudaStream_t s, LaunchLog& log);
+                         const float* bias, cudaStream_t s, LaunchLog& log,
+                         bool logits_ready = false);
+// Router logits for large batches on the tensor cores: splits router_w into
+// three bf16 planes [3, E, H] (planes) and multiplies them with x. xmap: 2-D
+// bf16 view {H, T} of x, wmap: {H, 3E} of planes, both box {64, 128} with
+// 128-byte swizzle.
+cudaError_t router_tc_setup();
+cudaError_t launch_router_logits_tc(const Dims& d, const float* router_w, uint16_t* planes,
+                                    const CUtensorMap& xmap, const CUtensorMap& wmap, float* logits,
+                                    unsigned* err, cudaStream_t s, LaunchLog& log);
 
 cudaError_t gemv_setup(int* ctas_per_sm);
 cudaError_t launch_gemv_gate_up(const Dims& d, const Routing& r, const GemvWeights& w,
@@ -78,13 +88,11 @@ cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& 
 
 // Tensor-core (tcgen05) expert GEMMs for large batches.
 struct TcWeights {
-  const uint16_t* scale_routed;  // bf16 group scales (global loads when !scale_tma)
+  const uint16_t* scale_routed;  // bf16 group scales [rows, K/128]
   const uint16_t* scale_shared;
-  // 2-D views {K/8 words, rows} of the packed weights, box {8 words, 128 rows}
+  // 2-D views {K/8 words, rows} of the packed weights, box {8 words, 128 rows},
+  // 32-byte swizzle
   CUtensorMap wq_r, wq_s;
-  // 2-D views {K/128, rows} of the scales, box {K/128, 128} (when scale_tma)
-  CUtensorMap ws_r, ws_s;
-  int scale_tma;
 };
 cudaError_t tc_setup(int* ctas_per_sm);
 // gate/up + SwiGLU: xmap is a 2-D bf16 view {H, rows} of Routing::xperm with

@@ -36,13 +36,18 @@ struct moe_w4a16_handle {
   // tensor-map cache keyed by the tensor pointers it was encoded for:
   // 0 w13_q, 1 w2_q, 2 sh_w13_q, 3 sh_w2_q (3-D, 1-group boxes), 4 w13_s, 5 w2_s,
   // 6 sh_w13_s, 7 sh_w2_s (scales), 8 w13_q, 9 w2_q, 10 sh_w13_q, 11 sh_w2_q
-  // (2-D, 8-group boxes), 12..15 the same weights in 128-row boxes and 16..19
-  // their scales in 128-row boxes (tensor-core experts)
-  static constexpr int kMaps = 20;
+  // (2-D, 8-group boxes), 12..15 the same weights in 128-row boxes
+  // (tensor-core experts)
+  static constexpr int kMaps = 16;
   const void* map_keys[kMaps] = {};
   CUtensorMap maps[kMaps];
   // views of the workspace's activation operands for the tensor-core experts
   CUtensorMap xmap, hmap;
+  // tensor-core router: bf16 planes of router_w and the view of this call's x
+  uint16_t* planes = nullptr;
+  CUtensorMap wmap_router, xmap_router;
+  const void* xmap_key = nullptr;
+  int xmap_rows = 0;
 };
 
 namespace {
@@ -127,6 +132,7 @@ Layout plan(const moe_w4a16_config& c) {
       rows * H * 2,          // 21 xperm
       (E + 2) * 4,           // 22 task3
       (E + 2) * 4,           // 23 task4
+      3 * E * H * 2,         // 24 router planes
   };
   Layout L;
   size_t o = 0;
@@ -221,20 +227,17 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType type, int esize, const void* b
 }
 
 // Tensor-core operands. Packed INT4 [rows, K/8] uint32 in boxes of 8 words x
-// 128 rows (one 64-wide K block of a 128-channel tile); its scales [rows,
-// K/128] in boxes of all K/128 groups x 128 rows; a bf16 activation matrix
-// [rows, cols] in boxes of 64 x 64 with the 128-byte swizzle the tensor core
-// reads.
+// 128 rows (one 64-wide K block of a 128-channel tile, 32-byte swizzle: the
+// two 16-byte halves of a row swap places on row bit 2); a bf16 activation
+// matrix [rows, cols] in boxes of 64 x 64 (or 128) rows with the 128-byte
+// swizzle the tensor core reads.
 int encode_int4_map_tc(CUtensorMap* m, const void* base, long long rows, int K) {
   return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, base, K / 8, rows, 8, 128,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "int4 tiles");
+                   CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "int4 tiles");
 }
-int encode_scale_map_tc(CUtensorMap* m, const void* base, long long rows, int K) {
-  return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, K / kGroup, rows, K / kGroup, 128,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "scale tiles");
-}
-int encode_act_map_tc(CUtensorMap* m, const void* base, long long cols, long long rows) {
-  return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, 64, 64,
+int encode_act_map_tc(CUtensorMap* m, const void* base, long long cols, long long rows,
+                      int box_rows = 64) {
+  return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, 64, box_rows,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "activations");
 }
 
@@ -243,8 +246,7 @@ int get_map(moe_w4a16_handle* h, int slot, const void* base, long long rows, int
   const int st = slot < 4    ? encode_int4_map(&h->maps[slot], base, rows, K)
                  : slot < 8  ? encode_scale_map(&h->maps[slot], base, rows, K)
                  : slot < 12 ? encode_int4_map2d(&h->maps[slot], base, rows, K)
-                 : slot < 16 ? encode_int4_map_tc(&h->maps[slot], base, rows, K)
-                             : encode_scale_map_tc(&h->maps[slot], base, rows, K);
+                             : encode_int4_map_tc(&h->maps[slot], base, rows, K);
   if (st == MOE_W4A16_OK) h->map_keys[slot] = base;
   return st;
 }
@@ -325,15 +327,17 @@ int moe_w4a16_create(const moe_w4a16_config* cfg, int device, moe_w4a16_handle**
     return st != MOE_W4A16_OK ? st : MOE_W4A16_ERR_CUDA;
   }
   h->decode_grid = h->num_sms * dec_per_sm;
-  // tensor-core experts: down tiles are 256 output channels wide; the scale
-  // boxes hold every K group of a row (at most 256)
-  h->tc_ok = cfg->hidden % 256 == 0 && cfg->hidden / kGroup <= 256 && cfg->inter / kGroup <= 256 &&
-             cfg->shared_inter / kGroup <= 256;
+  // tensor-core experts: down tiles are 256 output channels wide
+  h->tc_ok = cfg->hidden % 256 == 0;
   if ((cfg->flags & MOE_W4A16_FLAG_FORCE_TC) && !h->tc_ok) {
     delete h;
     return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
   }
   int tc_per_sm = 0;
+  if ((st = cuda_status(router_tc_setup())) != MOE_W4A16_OK) {
+    delete h;
+    return st;
+  }
   if ((st = cuda_status(tc_setup(&tc_per_sm))) != MOE_W4A16_OK || tc_per_sm < 1) {
     delete h;
     return st != MOE_W4A16_OK ? st : MOE_W4A16_ERR_CUDA;
@@ -374,10 +378,13 @@ int moe_w4a16_create(const moe_w4a16_config* cfg, int device, moe_w4a16_handle**
   r.xperm = reinterpret_cast<uint16_t*>(b + L.off[21]);
   r.task3 = reinterpret_cast<int*>(b + L.off[22]);
   r.task4 = reinterpret_cast<int*>(b + L.off[23]);
+  h->planes = reinterpret_cast<uint16_t*>(b + L.off[24]);
   if (h->tc_ok) {
     const long long rows = (long long)cfg->max_tokens * (cfg->top_k + 1);
     if ((st = encode_act_map_tc(&h->xmap, r.xperm, cfg->hidden, rows)) != MOE_W4A16_OK ||
-        (st = encode_act_map_tc(&h->hmap, h->h, h->hstride, rows)) != MOE_W4A16_OK) {
+        (st = encode_act_map_tc(&h->hmap, h->h, h->hstride, rows)) != MOE_W4A16_OK ||
+        (st = encode_act_map_tc(&h->wmap_router, h->planes, cfg->hidden, 3LL * cfg->num_experts,
+                                128)) != MOE_W4A16_OK) {
       moe_w4a16_destroy(h);
       return st;
     }
@@ -510,31 +517,24 @@ int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t T, const m
         return st;
       if ((st = get_map(h, 15, w->sh_w2_q, c.hidden, c.shared_inter)) != MOE_W4A16_OK) return st;
     }
-    if (scale_tma) {
-      if ((st = get_map(h, 16, w->w13_s, r13, c.hidden)) != MOE_W4A16_OK) return st;
-      if ((st = get_map(h, 17, w->w2_s, r2, c.inter)) != MOE_W4A16_OK) return st;
-      if (has_sh) {
-        if ((st = get_map(h, 18, w->sh_w13_s, 2LL * c.shared_inter, c.hidden)) != MOE_W4A16_OK)
-          return st;
-        if ((st = get_map(h, 19, w->sh_w2_s, c.hidden, c.shared_inter)) != MOE_W4A16_OK) return st;
-      }
-    }
     TcWeights t1, t2;
     t1.wq_r = h->maps[12];
     t1.wq_s = has_sh ? h->maps[14] : h->maps[12];
-    t1.ws_r = scale_tma ? h->maps[16] : h->maps[12];
-    t1.ws_s = scale_tma && has_sh ? h->maps[18] : t1.ws_r;
     t1.scale_routed = w->w13_s;
     t1.scale_shared = has_sh ? w->sh_w13_s : w->w13_s;
-    t1.scale_tma = scale_tma;
     t2.wq_r = h->maps[13];
     t2.wq_s = has_sh ? h->maps[15] : h->maps[13];
-    t2.ws_r = scale_tma ? h->maps[17] : h->maps[13];
-    t2.ws_s = scale_tma && has_sh ? h->maps[19] : t2.ws_r;
     t2.scale_routed = w->w2_s;
     t2.scale_shared = has_sh ? w->sh_w2_s : w->w2_s;
-    t2.scale_tma = scale_tma;
-    if ((e = launch_route(d, h->r, x, w->router_w, w->router_bias, s, h->log)) != cudaSuccess)
+    if (h->xmap_key != x || h->xmap_rows != T) {
+      if ((st = encode_act_map_tc(&h->xmap_router, x, c.hidden, T, 128)) != MOE_W4A16_OK) return st;
+      h->xmap_key = x;
+      h->xmap_rows = T;
+    }
+    if ((e = launch_router_logits_tc(d, w->router_w, h->planes, h->xmap_router, h->wmap_router,
+                                     h->r.logits, h->r.err, s, h->log)) != cudaSuccess)
+      return cuda_status(e);
+    if ((e = launch_route(d, h->r, x, w->router_w, w->router_bias, s, h->log, true)) != cudaSuccess)
       return cuda_status(e);
     if ((e = launch_tc_gate_up(d, h->r, t1, h->xmap, h->h, h->hstride, h->tc_grid, s, h->log)) !=
         cudaSuccess)

@@ -308,14 +308,6 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
   __shared__ float ws[32][64 + 4];
   const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  if (blockIdx.y == 0 && r.xperm) {
-    // the shared expert's rows of the tensor-core operand: x in the
-    // interleaved order, after the T*k routed rows
-    const int rows = min(64, d.T - t0);
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t0 * d.H);
-    uint4* dst = reinterpret_cast<uint4*>(r.xperm + (size_t)(d.T * d.k + t0) * d.H);
-    for (int i = threadIdx.x; i < rows * d.H / 8; i += blockDim.x) dst[i] = interleave8(src[i]);
-  }
 
   float acc[4][4] = {};
   for (int k0 = 0; k0 < d.H; k0 += 32) {
@@ -457,21 +449,41 @@ __global__ void __launch_bounds__(256) route_place_kernel(const uint16_t* __rest
     __syncthreads();
   }
   if (r.xperm) {
-    // routed rows of the tensor-core operand: x[t] at its expert-sorted row,
-    // in the interleaved order (one warp per row)
+    // the tensor-core operand: x[t] in the interleaved order at each of its
+    // k expert-sorted rows and at its shared-expert row T*k + t (one warp per
+    // token, each 16-byte chunk read once and written k + 1 times)
     const int h8 = d.H / 8;
-    for (int i = i0 + warp; i < i1; i += 8) {
-      const int pos = r.inv[i], t = i / d.k;
+    const int tend = min(d.T, (blockIdx.x + 1) * kTopkTokens);
+    for (int t = blockIdx.x * kTopkTokens + warp; t < tend; t += 8) {
+      // lane j < k holds the row of slot j, lane k the shared row
+      int myrow = 0;
+      if (lane < d.k) myrow = r.inv[t * d.k + lane];
+      else if (lane == d.k) myrow = d.T * d.k + t;
+      const int nd = d.k + (d.Is > 0 ? 1 : 0);
       const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d.H);
-      uint4* dst = reinterpret_cast<uint4*>(r.xperm + (size_t)pos * d.H);
-      for (int c = lane; c < h8; c += 32) dst[c] = interleave8(__ldg(src + c));
+      for (int c0 = 0; c0 < h8; c0 += 4 * 32) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + u * 32 + lane;
+          if (c < h8) v[u] = interleave8(__ldg(src + c));
+        }
+        for (int j = 0; j < nd; ++j) {
+          uint4* dst = reinterpret_cast<uint4*>(r.xperm + (size_t)__shfl_sync(0xffffffffu, myrow, j) * d.H);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < h8) dst[c] = v[u];
+          }
+        }
+      }
     }
   }
 }
 
 // ------------------------------------------------------------------ launcher
 cudaError_t launch_route(const Dims& d, const Routing& r, const uint16_t* x, const float* router_w,
-                         const float* bias, cudaStream_t s, LaunchLog& log) {
+                         const float* bias, cudaStream_t s, LaunchLog& log, bool logits_ready) {
   if (d.T <= kSmallT && !r.xperm) {
     log.begin("route_small", s);
     route_small_kernel<<<(d.E + 1) / 2, 256, 0, s>>>(x, router_w, bias, d, r);
@@ -479,9 +491,11 @@ cudaError_t launch_route(const Dims& d, const Routing& r, const uint16_t* x, con
     return cudaGetLastError();
   }
   const int nblk = (d.T + kTopkTokens - 1) / kTopkTokens;
-  log.begin("router_logits", s);
-  router_logits_kernel<<<dim3((d.T + 63) / 64, (d.E + 63) / 64), 256, 0, s>>>(x, router_w, d, r);
-  log.end(s);
+  if (!logits_ready) {
+    log.begin("router_logits", s);
+    router_logits_kernel<<<dim3((d.T + 63) / 64, (d.E + 63) / 64), 256, 0, s>>>(x, router_w, d, r);
+    log.end(s);
+  }
   log.begin("router_topk", s);
   router_topk_kernel<<<nblk, 256, 0, s>>>(bias, d, r);
   log.end(s);
