@@ -20,19 +20,21 @@
 //
 // Warp roles per CTA:
 //   warp 0     TMA producer of the weights: per 64-wide K block the two 128-row
-//              INT4 tiles (4 KB each, 32-byte swizzle) into a deep ring that
-//              the dequantisers free as soon as they have read a stage.
+//              INT4 tiles (4 KB each, 32-byte swizzle) into a ring that the
+//              dequantisers free as soon as they have read a stage.
 //   warp 1     TMEM owner (allocates all 512 columns) and MMA issuer: 4 K-steps
 //              x 2 tiles of tcgen05.mma kind::f16 (bf16 x bf16 -> fp32) per K
 //              block; commits release the activation and bf16 stages, the
 //              task's last one the accumulator.
-//   warp 2     TMA producer of the activations (64-row boxes, 128-byte swizzle).
+//   warp 2     TMA producer of the activations (64-row boxes, 128-byte swizzle)
+//              into four 32 KB stages: an activation tile takes about a
+//              microsecond to arrive, four MMA K blocks' worth.
 //   warps 3-10 dequantisers, one weight row per thread: INT4 -> bf16 (q * scale,
 //              one rounding) written in the canonical K-major 128-byte-swizzled
 //              layout tcgen05 reads; each thread fetches its row's group scale
 //              one group ahead with a plain load.
-//   warps 11-18 epilogue: tcgen05.ld of the accumulator (two warps per TMEM
-//              lane quarter), SwiGLU -> bf16 h, or fp32 y.
+//   warps 11-26 epilogue: tcgen05.ld of the accumulator (four warps per TMEM
+//              lane quarter, 16-column chunks), SwiGLU -> bf16 h, or fp32 y.
 // The activation operand (x rows in expert order, or h) is stored with each 8
 // consecutive values in the order (0,4)(1,5)(2,6)(3,7); the dequantiser emits
 // the weights in that same order, so no shuffle is needed on either side.
@@ -48,12 +50,12 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 19 * 32;
+constexpr int kThreads = 27 * 32;
 constexpr int kDqWarp0 = 3, kEpiWarp0 = 11;
 constexpr int kBK = 64;                               // K per block (one 128-byte swizzle atom)
 constexpr int kWStages = 4;
-constexpr int kBStages = 3;
-constexpr int kAbfStages = 3;
+constexpr int kBStages = 4;
+constexpr int kAbfStages = 2;
 constexpr int kInt4Tile = 128 * kBK / 2;              // 4 KB: 128 rows x 64 codes
 constexpr int kWB = 2 * kInt4Tile;                    // 8 KB
 constexpr int kBTile = kTcN * kBK * 2;                // 32 KB: 256 rows x 64 bf16
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.abf_empty[i], 1);
     }
     mbar_init(&s.acc_full, 1);
-    mbar_init(&s.acc_empty, 8);
+    mbar_init(&s.acc_empty, 16);
     mbar_init(&s.drain, 1);
     fence_mbar_init();
   }
@@ -313,7 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- dequantisers
     const int t256 = threadIdx.x - kDqWarp0 * 32;  // 0..255
     const int tile = t256 >> 7, row = t256 & 127;
-    // 32-byte swizzle of the INT4 tile: 16-byte halves swap on row bit 2
+    // 32-byte swizzle of the INT4 tile: the two 16-byte halves of a row swap
+    // places on row bit 2
     const uint32_t half0 = (uint32_t)((row >> 2) & 1) << 4;
     int wstage = 0, astage = 0;
     uint32_t wph = 0, aph = 0;
@@ -394,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;                      // TMEM lane quarter this warp may access
-    const int half = (warp - kEpiWarp0) >> 2;    // 32-column chunks half, half + 2, ...
+    const int cg = (warp - kEpiWarp0) >> 2;      // 16-column chunks cg, cg + 4, ...
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const int ch = q * 32 + lane;                // channel within a 128-row tile
     int it = 0;
@@ -402,17 +405,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TcTask t = decode_task<MODE>(p, tau, n_sh, n_act);
       if (!warp_wait(&s.acc_full, it & 1, err)) break;
       tc_fence_after();
-      for (int c0 = half * 32; c0 < t.n; c0 += 64) {
-        float v0[32], v1[32];
-        tmem_ld32(tmem + lane_base + c0, v0);
-        tmem_ld32(tmem + lane_base + 256 + c0, v1);
+      for (int c0 = cg * 16; c0 < t.n; c0 += 64) {
+        float v0[16], v1[16];
+        tmem_ld16(tmem + lane_base + c0, v0);
+        tmem_ld16(tmem + lane_base + 256 + c0, v1);
         const int cn = t.n - c0;
         if (MODE == 1) {
           const int n = t.chan0 + ch;
           const int pos = (n & ~7) | ((n & 3) << 1) | ((n >> 2) & 1);
           uint16_t* hp = p.hout + (size_t)(t.brow0 + c0) * p.hstride + pos;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
+          for (int j = 0; j < 16; ++j)
             if (j < cn) {
               const float g = v0[j];
               hp[(size_t)j * p.hstride] = f32_to_bf16_bits(__fdividef(g, 1.0f + __expf(-g)) * v1[j]);
@@ -420,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           float* yr = p.yout + (size_t)(t.brow0 + c0) * d.H + t.chan0 + ch;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
+          for (int j = 0; j < 16; ++j)
             if (j < cn) {
               yr[(size_t)j * d.H] = v0[j];
               yr[(size_t)j * d.H + 128] = v1[j];
