@@ -28,11 +28,15 @@
 //    m16n8k16 with weights as A and up to 8 rows as B, group scales applied
 //    in fp32. At the end of a task each warp drops its partial sums into a
 //    slot and moves on.
-//  * 1 producer warp: decodes tasks and fills a 5-stage ring (2-D TMA boxes
-//    of 16 rows x 512 B per tile, scale boxes, bulk copies of the activation
-//    rows) with a descriptor per stage. Down tasks need the h rows of their
-//    (expert, pass): their weights are prefetched at once, their h copies wait
-//    on a per-(expert, pass) completion counter.
+//  * 1 weight producer warp: decodes tasks and fills a 5-stage ring (2-D TMA
+//    boxes of 16 rows x 512 B per tile, scale boxes) with a descriptor per
+//    stage; it only ever waits for free stages, so the weight stream never
+//    stops on a dependency.
+//  * 1 activation warp: in ring order, copies each stage's activation rows
+//    (x for gate/up, h for down) into the stage (1-D bulk copies). Down tasks
+//    need the h rows of their (expert, pass): it polls the completion counters
+//    of every active (expert, pass) at once (lanes in parallel, one round trip)
+//    and keeps the finished ones in a shared-memory bitmap.
 //  * 4 epilogue warps, one per slot: fixed-order reduction of the 16 partial
 //    sums, SwiGLU -> bf16 h (then a release-add on the (expert, pass)
 //    counter) or fp32 y (then an acq_rel ticket per channel tile; the task
@@ -55,10 +59,11 @@ namespace {
 constexpr int kCW = 16;                      // consumer warps
 constexpr int kEW = 4;                       // epilogue warps (= slots)
 constexpr int kRW = 4;                       // router warps
-constexpr int kProd = kCW;                   // producer warp index
-constexpr int kEpi0 = kCW + 1;               // first epilogue warp
+constexpr int kProd = kCW;                   // weight producer warp index
+constexpr int kActs = kCW + 1;               // activation warp index
+constexpr int kEpi0 = kCW + 2;               // first epilogue warp
 constexpr int kRtr0 = kEpi0 + kEW;           // first router warp
-constexpr int kThreads = (kCW + 1 + kEW + kRW) * 32;
+constexpr int kThreads = (kCW + 2 + kEW + kRW) * 32;
 constexpr int kR = 8;                        // rows per pass (MMA N)
 constexpr int kS = 5;                        // ring stages
 constexpr int kWB = 2 * 16 * 512;            // 2 tiles x 16 rows x 512 B (8 K-groups)
@@ -67,12 +72,13 @@ constexpr int kXS = 8 * 256 + 64;            // one activation row (8 groups bf1
 constexpr int kXO = kWB + kSB;
 constexpr int kStageB = (kXO + kR * kXS + 1023) / 1024 * 1024;
 constexpr int kMaxPass = (kSmallT + kR - 1) / kR;  // passes per expert at most
+constexpr int kPairs = (kMaxExperts + 1) * kMaxPass;  // (expert, pass) counters
 constexpr int kItems = kSmallT * kMaxTopK;
 
 enum { kFirst = 1, kLast = 2, kEnd = 4, kShared = 8, kDown = 16 };
 
 struct Desc {
-  int flags, g0, gcnt, ngroups, tile, r0, nr, rowA0, rowA1, cnt, pad[2];
+  int flags, g0, gcnt, ngroups, tile, r0, nr, rowA0, rowA1, cnt, pad[2];  // cnt: (expert, pass)
 };
 
 struct Smem {
@@ -95,6 +101,8 @@ struct Smem {
   int meta[4];                          // n_act, routed gate/up tasks, routed down tasks
   uint64_t full[kS];
   uint64_t empty[kS];
+  uint64_t desc_ready[kS];              // weight producer -> activation warp
+  unsigned pair_done[(kPairs + 31) / 32];  // finished (expert, pass) gate/up work
   uint64_t slot_full[kEW];
   uint64_t slot_free[kEW];
   uint64_t route_ready;
@@ -568,7 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kS; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], kCW);
+      mbar_init(&s.desc_ready[i], 1);
     }
+    for (int i = 0; i < (kPairs + 31) / 32; ++i) s.pair_done[i] = 0u;
     for (int i = 0; i < kEW; ++i) {
       mbar_init(&s.slot_full[i], kCW);
       mbar_init(&s.slot_free[i], 1);
@@ -584,60 +594,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   cnt.r1 = cnt.r2 = cnt.n_act = 0;
 
   if (warp == kProd) {
-    // ---------------------------------------------------------------- producer
+    // ---------------------------------------------------------------- weight producer
     bool known = false, stop = false;
     int stage = 0;
     uint32_t phase = 0;
-    // FIFO of stages whose h copies wait for their (expert, pass) counter
-    int pn = 0;
-    int q_stage[kS], q_g0[kS];
-    Task q_task[kS];
-
-    auto issue_acts = [&](int st_i, const Task& t, int g0) {
-      if (lane < t.nr) {
-        const int r = t.r0 + lane;
-        const uint16_t* src;
-        if (!t.down)
-          src = p.x + (size_t)(t.shared ? r - d.T * d.k : s.perm_s[r]) * d.H;
-        else
-          src = p.h + (size_t)r * p.hstride;
-        bulk_copy(smem_u32(s.stage[st_i] + kXO + lane * kXS), src + g0 * kGroup,
-                  min(8, t.ngroups - g0) * 256, &s.full[st_i]);
-      }
-    };
-    auto dep_ready = [&](const Task& t, bool block) -> int {
-      int ok = 1;
-      const int* c = p.done1 + t.e * kMaxPass + t.pass;
-      if (lane == 0)
-        ok = block ? (wait_counter(c, t.cnt_target, err) ? 1 : 0)
-                   : (ld_acquire(c) >= t.cnt_target ? 1 : 0);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (ok) {
-        // every lane that copies h orders its copies after the producers' writes
-        (void)ld_acquire(c);
-        fence_proxy_async();
-      }
-      return ok;
-    };
-    // issue h copies of queued stages whose dependency is met (oldest first)
-    auto drain = [&](bool block) -> bool {
-      while (pn > 0) {
-        const int ok = dep_ready(q_task[0], block);
-        if (!ok) {
-          if (block) return false;
-          break;
-        }
-        issue_acts(q_stage[0], q_task[0], q_g0[0]);
-        for (int i = 1; i < pn; ++i) {
-          q_stage[i - 1] = q_stage[i];
-          q_g0[i - 1] = q_g0[i];
-          q_task[i - 1] = q_task[i];
-        }
-        --pn;
-      }
-      return true;
-    };
-
     if (lane == 0) {
       prefetch_tmap(&tm13r);
       prefetch_tmap(&tm13s);
@@ -650,6 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ok = 1;
         if (lane == 0) ok = dwait(&s.route_ready, 0, err) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        __syncwarp();  // orders every lane's routing reads after lane 0's wait
         cnt.n_act = s.meta[0];
         cnt.r1 = s.meta[1];
         cnt.r2 = s.meta[2];
@@ -657,75 +618,123 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const Task t = task_at(s, d, cnt, tau);
       if (t.ngroups == 0) break;
-      const CUtensorMap* tm = t.down ? (t.shared ? &tm2s : &tm2r) : (t.shared ? &tm13s : &tm13r);
-      const CUtensorMap* ts = t.down ? (t.shared ? &ts2s : &ts2r) : (t.shared ? &ts13s : &ts13r);
-      for (int g0 = 0; g0 < t.ngroups; g0 += 8) {
-        const int gcnt = min(8, t.ngroups - g0);
-        // Consumers take stages in ring order: a queued down stage whose h
-        // copies are not issued yet holds every later stage back. Resolve the
-        // queue (blocking on the oldest dependency, which only needs earlier
-        // gate/up tasks) before waiting for a slot that is not free yet.
-        if (pn > 0) {
-          drain(false);
-          if (pn > 0) {
-            int free_slot = 0;
-            if (lane == 0) free_slot = mbar_try_wait(&s.empty[stage], phase ^ 1u) ? 1 : 0;
-            if (!__shfl_sync(0xffffffffu, free_slot, 0) && !drain(true)) {
-              stop = true;
-              break;
-            }
+      if (lane == 0) {
+        const CUtensorMap* tm = t.down ? (t.shared ? &tm2s : &tm2r) : (t.shared ? &tm13s : &tm13r);
+        const CUtensorMap* ts = t.down ? (t.shared ? &ts2s : &ts2r) : (t.shared ? &ts13s : &ts13r);
+        for (int g0 = 0; g0 < t.ngroups; g0 += 8) {
+          const int gcnt = min(8, t.ngroups - g0);
+          if (!dwait(&s.empty[stage], phase ^ 1u, err)) {
+            stop = true;
+            break;
           }
-        }
-        int ok = 1;
-        if (lane == 0) {
-          ok = dwait(&s.empty[stage], phase ^ 1u, err) ? 1 : 0;
-          if (ok) {
-            Desc& ds = s.desc[stage];
-            ds.flags = (g0 == 0 ? kFirst : 0) | (g0 + 8 >= t.ngroups ? kLast : 0) |
-                       (t.shared ? kShared : 0) | (t.down ? kDown : 0);
-            ds.g0 = g0;
-            ds.gcnt = gcnt;
-            ds.ngroups = t.ngroups;
-            ds.tile = t.tile;
-            ds.r0 = t.r0;
-            ds.nr = t.nr;
-            ds.rowA0 = t.rowA0;
-            ds.rowA1 = t.rowA1;
-            ds.cnt = t.e * kMaxPass + t.pass;
-            // a TMA box always delivers its full size (out-of-range parts are zero-filled)
-            mbar_arrive_expect_tx(&s.full[stage], kWB + (scale_tma ? kSB : 0) + t.nr * gcnt * 256);
-            uint8_t* st = s.stage[stage];
-            tma_2d(smem_u32(st), tm, &s.full[stage], g0 * 16, t.rowA0);
-            tma_2d(smem_u32(st + kWB / 2), tm, &s.full[stage], g0 * 16, t.rowA1);
-            if (scale_tma) {
-              tma_2d(smem_u32(st + kWB), ts, &s.full[stage], g0, t.rowA0);
-              tma_2d(smem_u32(st + kWB + kSB / 2), ts, &s.full[stage], g0, t.rowA1);
-            }
+          Desc& ds = s.desc[stage];
+          ds.flags = (g0 == 0 ? kFirst : 0) | (g0 + 8 >= t.ngroups ? kLast : 0) |
+                     (t.shared ? kShared : 0) | (t.down ? kDown : 0);
+          ds.g0 = g0;
+          ds.gcnt = gcnt;
+          ds.ngroups = t.ngroups;
+          ds.tile = t.tile;
+          ds.r0 = t.r0;
+          ds.nr = t.nr;
+          ds.rowA0 = t.rowA0;
+          ds.rowA1 = t.rowA1;
+          ds.cnt = t.e * kMaxPass + t.pass;
+          // the activation warp copies nr rows into the stage; a TMA box always
+          // delivers its full size (out-of-range parts are zero-filled)
+          mbar_arrive_expect_tx(&s.full[stage], kWB + (scale_tma ? kSB : 0) + t.nr * gcnt * 256);
+          uint8_t* st = s.stage[stage];
+          tma_2d(smem_u32(st), tm, &s.full[stage], g0 * 16, t.rowA0);
+          tma_2d(smem_u32(st + kWB / 2), tm, &s.full[stage], g0 * 16, t.rowA1);
+          if (scale_tma) {
+            tma_2d(smem_u32(st + kWB), ts, &s.full[stage], g0, t.rowA0);
+            tma_2d(smem_u32(st + kWB + kSB / 2), ts, &s.full[stage], g0, t.rowA1);
           }
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) {
-          stop = true;
-          break;
-        }
-        if (!t.down) {
-          issue_acts(stage, t, g0);
-        } else {
-          q_stage[pn] = stage;
-          q_g0[pn] = g0;
-          q_task[pn] = t;
-          ++pn;
-          drain(false);
-        }
-        if (++stage == kS) {
-          stage = 0;
-          phase ^= 1u;
+          mbar_arrive(&s.desc_ready[stage]);
+          if (++stage == kS) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
+      stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
+      stage = __shfl_sync(0xffffffffu, stage, 0);
+      phase = __shfl_sync(0xffffffffu, phase, 0);
     }
-    if (!stop) stop = !drain(true);
     if (lane == 0 && !stop && dwait(&s.empty[stage], phase ^ 1u, err)) {
       s.desc[stage].flags = kEnd;
       mbar_arrive(&s.full[stage]);
+      mbar_arrive(&s.desc_ready[stage]);
+    }
+  } else if (warp == kActs) {
+    // ---------------------------------------------------------------- activation rows
+    int stage = 0;
+    uint32_t phase = 0;
+    bool routed_known = false;
+    // poll every active (expert, pass) gate/up counter once (lanes in parallel)
+    // and record the finished ones; returns true when pair `want` is finished
+    auto poll_pairs = [&](int want) -> bool {
+      const int n_sh = d.Is > 0 ? passes_of(d.T) : 0;
+      const int n_act = routed_known ? s.meta[0] : 0;
+      for (int i = lane; i < n_sh + n_act * kMaxPass; i += 32) {
+        int e, pass, target;
+        if (i < n_sh) {
+          e = d.E;
+          pass = i;
+          target = d.Is / kTile1;
+        } else {
+          const int a = (i - n_sh) / kMaxPass;
+          e = s.active[a];
+          pass = (i - n_sh) - a * kMaxPass;
+          if (pass >= passes_of(s.offsets[e + 1] - s.offsets[e])) continue;
+          target = d.I / kTile1;
+        }
+        const int id = e * kMaxPass + pass;
+        if (s.pair_done[id >> 5] & (1u << (id & 31))) continue;
+        if (ld_acquire(p.done1 + id) >= target) atomicOr(&s.pair_done[id >> 5], 1u << (id & 31));
+      }
+      __syncwarp();
+      return (s.pair_done[want >> 5] >> (want & 31)) & 1u;
+    };
+    for (;;) {
+      if (!__all_sync(0xffffffffu, dwait(&s.desc_ready[stage], phase, err))) break;
+      const Desc ds = s.desc[stage];
+      if (ds.flags & kEnd) break;
+      if (!routed_known && !(ds.flags & kShared)) routed_known = true;  // routing is in smem
+      const bool down = (ds.flags & kDown) != 0;
+      if (down && !((s.pair_done[ds.cnt >> 5] >> (ds.cnt & 31)) & 1u)) {
+        // wait for the gate/up work of this (expert, pass) anywhere in the grid
+        const uint64_t t0 = global_ns();
+        bool got = poll_pairs(ds.cnt);
+        while (!got) {
+          __nanosleep(128);
+          if (aborted(err)) break;
+          if (global_ns() - t0 > kWaitLimitNs) {
+            if (lane == 0) atomicOr(err, kErrTimeout);
+            break;
+          }
+          got = poll_pairs(ds.cnt);
+        }
+        if (!got) break;
+      }
+      if (down) {
+        // every lane that copies h orders its copies after the acquires above
+        __syncwarp();
+        fence_proxy_async();
+      }
+      if (lane < ds.nr) {
+        const int r = ds.r0 + lane;
+        const uint16_t* src;
+        if (!down)
+          src = p.x + (size_t)((ds.flags & kShared) ? r - d.T * d.k : s.perm_s[r]) * d.H;
+        else
+          src = p.h + (size_t)r * p.hstride;
+        bulk_copy(smem_u32(s.stage[stage] + kXO + lane * kXS), src + ds.g0 * kGroup, ds.gcnt * 256,
+                  &s.full[stage]);
+      }
+      if (++stage == kS) {
+        stage = 0;
+        phase ^= 1u;
+      }
     }
   } else if (warp < kCW) {
     // ---------------------------------------------------------------- consumers
