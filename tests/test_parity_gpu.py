@@ -157,6 +157,9 @@ def test_tiny_deterministic_and_batch_invariant(tiny):
     np.testing.assert_array_equal(a, b)
     c, _ = _run(obj, layer.x[:5])
     np.testing.assert_array_equal(c, a[:5])
+    # tiny batches score with more warps; the logits' summation order is fixed
+    c, _ = _run(obj, layer.x[:3])
+    np.testing.assert_array_equal(c, a[:3])
     obj.close()
 
 

@@ -97,6 +97,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, but the thread may be suspended (up to about a microsecond)
+// until the phase completes instead of returning at once: waiting warps then
+// leave the issue slots to the warps that have work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(1000u)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -110,8 +125,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if ((i & 15u) == 0 && global_ns() - t0 > kWaitLimitNs) {
       atomicOr(err, kErrTimeout);
       return false;
     }
@@ -156,6 +171,17 @@ __device__ __forceinline__ uint32_t int4_pair_to_bf16x2(uint32_t word) {
   const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
   b = __hsub2(b, off);
   return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// The same two codes as bf16 128 + u (exact), without the subtraction: a
+// caller that subtracts 136 * sum(x) from the dot product afterwards gets the
+// same result up to fp32 rounding.
+template <int J>
+__device__ __forceinline__ uint32_t int4_pair_to_bf16x2_offset(uint32_t word) {
+  uint32_t v;
+  const uint32_t w = word >> (4 * J);
+  asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(v) : "r"(w), "r"(0x000F000Fu), "r"(0x43004300u));
+  return v;
 }
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {

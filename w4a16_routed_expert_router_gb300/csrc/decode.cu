@@ -18,20 +18,29 @@
 //
 // Warp roles (one CTA per SM):
 //  * 4 router warps: every CTA scores one or two experts for all tokens
-//    (fp32), publishes the logits, waits until every CTA has (a counter),
-//    then computes the whole routing itself in shared memory (top-k,
-//    histogram, scan, stable permutation, task lists). Computing it
-//    redundantly per CTA keeps the critical path at two global round trips,
-//    and it overlaps the shared expert's work, which needs no routing.
+//    (fp32; the epilogue warps, idle until the first task ends, help: 8 warps
+//    hold a K slice of both router rows in registers and stream the tokens),
+//    publishes the logits, waits until every CTA has (a counter), then
+//    computes the whole routing itself in shared memory (top-k, histogram,
+//    scan, stable permutation, task lists). Computing it redundantly per CTA
+//    keeps the critical path at two global round trips, and it overlaps the
+//    shared expert's work, which needs no routing.
 //  * 16 consumer warps stream stages from the start: warp w takes K-group
 //    (w % 8) of tile (w / 8); exact INT4 -> bf16 in registers, mma.sync
 //    m16n8k16 with weights as A and up to 8 rows as B, group scales applied
 //    in fp32. At the end of a task each warp drops its partial sums into a
-//    slot and moves on.
-//  * 1 weight producer warp: decodes tasks and fills a 5-stage ring (2-D TMA
+//    slot and moves on. Routed gate/up stages skip two steps: their x rows
+//    come pre-interleaved, and the weights stay 136 + q (one op per code
+//    pair) with 136 * sum(x over the group) taken off each group's dot
+//    product; every CTA interleaves and sums its share of the tokens once per
+//    forward, before the logits are published.
+//  * 1 weight producer warp: decodes tasks and fills a ring of stages (2-D TMA
 //    boxes of 16 rows x 512 B per tile, scale boxes) with a descriptor per
 //    stage; it only ever waits for free stages, so the weight stream never
-//    stops on a dependency.
+//    stops on a dependency. A stage holds the weights plus room for the
+//    pass's activation rows (min(T, 8)), so a small batch gets more stages:
+//    at one token about 11 stages (176 KB of weights in flight per SM) instead
+//    of 5, enough to cover the ~1.5 us a weight box takes to arrive.
 //  * 1 activation warp: in ring order, copies each stage's activation rows
 //    (x for gate/up, h for down) into the stage (1-D bulk copies). Down tasks
 //    need the h rows of their (expert, pass): it polls the completion counters
@@ -64,50 +73,57 @@ constexpr int kActs = kCW + 1;               // activation warp index
 constexpr int kEpi0 = kCW + 2;               // first epilogue warp
 constexpr int kRtr0 = kEpi0 + kEW;           // first router warp
 constexpr int kThreads = (kCW + 2 + kEW + kRW) * 32;
+constexpr int kSW = kRW + kEW;               // warps that score experts (router + epilogue)
 constexpr int kR = 8;                        // rows per pass (MMA N)
-constexpr int kS = 5;                        // ring stages
+constexpr int kMaxS = 12;                    // ring stages at most (the count depends on T)
 constexpr int kWB = 2 * 16 * 512;            // 2 tiles x 16 rows x 512 B (8 K-groups)
 constexpr int kSB = 2 * 16 * 16;             // 2 tiles x 16 rows x 8 bf16 scales
 constexpr int kXS = 8 * 256 + 64;            // one activation row (8 groups bf16) + pad
 constexpr int kXO = kWB + kSB;
-constexpr int kStageB = (kXO + kR * kXS + 1023) / 1024 * 1024;
+constexpr int kSmemMax = 227 * 1024;         // opt-in shared memory of one CTA
 constexpr int kMaxPass = (kSmallT + kR - 1) / kR;  // passes per expert at most
 constexpr int kPairs = (kMaxExperts + 1) * kMaxPass;  // (expert, pass) counters
 constexpr int kItems = kSmallT * kMaxTopK;
 
-enum { kFirst = 1, kLast = 2, kEnd = 4, kShared = 8, kDown = 16 };
+enum { kFirst = 1, kLast = 2, kEnd = 4, kShared = 8, kDown = 16, kPre = 32 };
+constexpr int kXSumO = 8 * 256;              // group sums of a row, in its slot's padding
 
 struct Desc {
   int flags, g0, gcnt, ngroups, tile, r0, nr, rowA0, rowA1, cnt, pad[2];  // cnt: (expert, pass)
 };
 
 struct Smem {
-  uint8_t stage[kS][kStageB];
   float4 red[kEW][kCW * 32];            // task-end partial sums, one slot per epilogue warp
-  float part[2][kRW][kSmallT];          // router: per-warp partial logits of 2 experts
+  float part[2][kSW][kSmallT];          // router: per-warp partial logits of 2 experts
   float bias_s[kMaxExperts];
   Desc slot_desc[kEW];
-  Desc desc[kS];
+  Desc desc[kMaxS];
   int ids_s[kItems];
   float wts_s[kItems];
   int perm_s[kItems];
   int inv_s[kItems];
   int counts_s[kMaxExperts];
+  int run_s[kMaxExperts];               // router: running row count per expert
   int active[kMaxExperts + 2];
   int pre1[kMaxExperts + 2];
   int pre2[kMaxExperts + 2];
   int offsets[kMaxExperts + 2];
   int4 scan[kRW];
   int meta[4];                          // n_act, routed gate/up tasks, routed down tasks
-  uint64_t full[kS];
-  uint64_t empty[kS];
-  uint64_t desc_ready[kS];              // weight producer -> activation warp
+  uint64_t full[kMaxS];
+  uint64_t empty[kMaxS];
+  uint64_t desc_ready[kMaxS];           // weight producer -> activation warp
   unsigned pair_done[(kPairs + 31) / 32];  // finished (expert, pass) gate/up work
   uint64_t slot_full[kEW];
   uint64_t slot_free[kEW];
   uint64_t route_ready;
   int flag;
 };
+
+// The stage ring follows the fixed part of shared memory: nst stages of
+// stage_bytes each, sized at launch for the batch (a stage holds the weight
+// and scale boxes plus min(T, kR) activation rows).
+constexpr int kStageOff = (int)((sizeof(Smem) + 1023) / 1024 * 1024);
 
 struct DecodeParams {
   Dims d;
@@ -119,14 +135,19 @@ struct DecodeParams {
   const uint16_t* s13_shared;
   const uint16_t* s2_routed;
   const uint16_t* s2_shared;
-  uint16_t* h;                  // [rows, hstride] bf16, interleaved
+  uint16_t* xi;                 // [T, H] bf16: x interleaved, chunks transposed (chunk_t)
+  float* xs;                    // [T, xs_stride] fp32: sum of x over each K group
+  int xs_stride;                // H / 128 rounded up to 8 (32-byte rows)
+  uint16_t* h;                  // [rows, hstride] bf16, interleaved, chunks transposed
   int hstride;
   float* y;                     // [rows, H] fp32
   uint16_t* out;                // [T, H] bf16
   int* done1;                   // [(E + 1) * kMaxPass] gate/up tasks done per (expert, pass)
   int* tile_cnt;                // [H / 32] down tasks done per channel tile
-  unsigned* sync;               // [4]: logits ticket, (unused), exit ticket
+  unsigned* sync;               // [4]: logits ticket, x-interleave ticket, exit ticket
   int scale_tma;
+  int nst;                      // ring stages
+  int stage_bytes;              // bytes per stage (a multiple of 1024)
 };
 
 struct Task {
@@ -148,8 +169,8 @@ __device__ __forceinline__ bool dwait(uint64_t* bar, uint32_t parity, unsigned* 
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if ((i & 15u) == 0) {
       if (aborted(err)) return false;
       if (global_ns() - t0 > kWaitLimitNs) {
         atomicOr(err, kErrTimeout);
@@ -220,6 +241,53 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
   return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
 }
 
+// Activation rows the consumers read with the transposed addressing (the
+// interleaved x of routed gate/up stages, and h) store 16-byte chunk w of each
+// K group (w = 4c + m: lane column c, MMA step m) at position 4m + c.
+__device__ __forceinline__ int chunk_t(int w) { return ((w & 3) << 2) | (w >> 2); }
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// The 8 MMA steps of one K group of one stage (4 independent chains). OFFSET:
+// the A operand holds 136 + q (the caller corrects with the x group sums).
+template <bool OFFSET>
+__device__ __forceinline__ void stage_mma(const uint4& wA, const uint4& wB, const uint4 (&b)[4],
+                                          float (&t4)[4][4]) {
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t ra = word_of(wA, m), rb = word_of(wB, m);
+    uint32_t a[4];
+    if (OFFSET) {
+      a[0] = int4_pair_to_bf16x2_offset<0>(ra);
+      a[1] = int4_pair_to_bf16x2_offset<0>(rb);
+      a[2] = int4_pair_to_bf16x2_offset<1>(ra);
+      a[3] = int4_pair_to_bf16x2_offset<1>(rb);
+    } else {
+      a[0] = int4_pair_to_bf16x2<0>(ra);
+      a[1] = int4_pair_to_bf16x2<0>(rb);
+      a[2] = int4_pair_to_bf16x2<1>(ra);
+      a[3] = int4_pair_to_bf16x2<1>(rb);
+    }
+    mma_bf16_16816(t4[(2 * m) & 3], a, b[m].x, b[m].y, t4[(2 * m) & 3]);
+    if (OFFSET) {
+      a[0] = int4_pair_to_bf16x2_offset<2>(ra);
+      a[1] = int4_pair_to_bf16x2_offset<2>(rb);
+      a[2] = int4_pair_to_bf16x2_offset<3>(ra);
+      a[3] = int4_pair_to_bf16x2_offset<3>(rb);
+    } else {
+      a[0] = int4_pair_to_bf16x2<2>(ra);
+      a[1] = int4_pair_to_bf16x2<2>(rb);
+      a[2] = int4_pair_to_bf16x2<3>(ra);
+      a[3] = int4_pair_to_bf16x2<3>(rb);
+    }
+    mma_bf16_16816(t4[(2 * m + 1) & 3], a, b[m].z, b[m].w, t4[(2 * m + 1) & 3]);
+  }
+}
+
 // ------------------------------------------------------------ task decode
 struct Counts {
   int sh1, r1, sh2, r2, n_act;
@@ -287,62 +355,70 @@ __device__ __forceinline__ Task task_at(const Smem& s, const Dims& d, const Coun
   return t;
 }
 
-// ------------------------------------------------------------ router (consumers)
-// Top-k of one token from its logits in global memory (lane l holds experts
-// l, l+32, ...); lanes 0..k-1 return the chosen expert (descending sel, ties
-// -> lower index) and its renormalised unbiased score.
-__device__ __forceinline__ void warp_topk(const float* logit_row, const float* bias, int E, int k,
+// ------------------------------------------------------------ router
+constexpr int kPer = kMaxExperts / 32;  // logits per lane
+
+// Order-preserving key of a finite float (larger float -> larger key; key 0
+// stays below every float and marks a taken candidate).
+__device__ __forceinline__ unsigned fkey(float f) {
+  const unsigned u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Top-k of one token whose logits lane l holds for experts l, l + 32, ...;
+// lanes 0..k-1 return the chosen expert (descending sel, ties -> lower index)
+// and its renormalised unbiased score. A round is two warp reductions: the
+// largest selection key, then the lowest expert index among the lanes holding
+// it.
+__device__ __forceinline__ void warp_topk(const float (&lg)[kPer], const float* bias, int E, int k,
                                           int lane, int* out_id, float* out_w) {
-  constexpr int kPer = kMaxExperts / 32;
-  float sel[kPer], sc[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = lane + 32 * i;
-    sc[i] = (e < E) ? __ldcg(logit_row + e) : 0.f;
-  }
+  float sc[kPer];
+  unsigned key[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int e = lane + 32 * i;
     if (e < E) {
-      const float s = 1.0f / (1.0f + expf(-sc[i]));
-      sc[i] = s;
-      sel[i] = s + bias[e];
+      sc[i] = 1.0f / (1.0f + expf(-lg[i]));
+      key[i] = fkey(sc[i] + bias[e]);
     } else {
-      sel[i] = -INFINITY;
+      sc[i] = 0.f;
+      key[i] = 0u;
     }
   }
+  // this lane's best remaining candidate (lowest i among equal keys)
+  auto local_best = [&](unsigned& bk, int& bi) {
+    bk = key[0];
+    bi = 0;
+#pragma unroll
+    for (int i = 1; i < kPer; ++i)
+      if (key[i] > bk) {
+        bk = key[i];
+        bi = i;
+      }
+  };
+  unsigned bk;
+  int bi;
+  local_best(bk, bi);
   float chosen_s = 0.f;
   int chosen_e = -1;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = lane + 32 * i;
-      if (sel[i] > bv || (sel[i] == bv && e < be)) {
-        bv = sel[i];
-        be = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
+    const unsigned m = __reduce_max_sync(0xffffffffu, bk);
+    const unsigned cand = bk == m ? (unsigned)(lane + 32 * bi) : 0xffffffffu;
+    const unsigned win = __reduce_min_sync(0xffffffffu, cand);
+    const int wl = (int)(win & 31u), wi = (int)(win >> 5);
     float ws = 0.f;
+    if (lane == wl) {
 #pragma unroll
-    for (int i = 0; i < kPer; ++i)
-      if (lane + 32 * i == be) {
-        ws = sc[i];
-        sel[i] = -INFINITY;
-      }
-    ws = __shfl_sync(0xffffffffu, ws, be & 31);
+      for (int i = 0; i < kPer; ++i)
+        if (i == wi) {
+          ws = sc[i];
+          key[i] = 0u;
+        }
+      local_best(bk, bi);
+    }
+    ws = __shfl_sync(0xffffffffu, ws, wl);
     if (lane == j) {
-      chosen_e = be;
+      chosen_e = (int)win;
       chosen_s = ws;
     }
   }
@@ -350,6 +426,14 @@ __device__ __forceinline__ void warp_topk(const float* logit_row, const float* b
   for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, chosen_s, j);
   *out_id = chosen_e;
   *out_w = chosen_s / sum;
+}
+
+__device__ __forceinline__ void load_logits(const float* row, int E, int lane, float (&lg)[kPer]) {
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    lg[i] = e < E ? __ldcg(row + e) : 0.f;
+  }
 }
 
 // Exclusive scan of four ints over the 128 router threads (t = router thread).
@@ -389,85 +473,164 @@ __device__ __forceinline__ int4 rscan4(int4 v, int t, int4* scr, int4* total) {
                    base.w + inc.w - v.w);
 }
 
+// Warps that score experts: the router warps, joined by the epilogue warps
+// when the batch is tiny (they are free until the first task ends, which
+// takes longer than scoring a few tokens; at larger batches scoring would hold
+// them up).
+__device__ __forceinline__ int scoring_warps(const Dims& d) { return d.T <= 4 ? kSW : kRW; }
+
+// named barrier of the scoring warps
+__device__ __forceinline__ void sbar(int nsw) {
+  asm volatile("bar.sync 2, %0;" ::"r"(nsw * 32) : "memory");
+}
+
+// Logits of this CTA's experts (e = b and b + G, for all tokens) by the nsw
+// scoring warps. K is cut into kSW slices whatever the batch size, so a
+// token's logits do not depend on the batch; scoring warp w takes slices w,
+// w + nsw, ... Per slice each lane keeps its share of both router rows in
+// registers (up to 4 float4 each; larger slices go in chunks) and streams the
+// tokens' x through, two tokens per round trip; the slice partials are summed
+// in slice order.
+__device__ void score_experts(Smem& s, const DecodeParams& p, int sw) {
+  const Dims& d = p.d;
+  const int nsw = scoring_warps(d);
+  const int lane = threadIdx.x & 31, tid = sw * 32 + lane;
+  const int kw = d.H / kSW;   // K slice (a multiple of 16)
+  const int nf = kw / 4;      // float4 of the slice
+  for (int eb = blockIdx.x; eb < d.E; eb += 2 * gridDim.x) {
+    const int e0 = eb, e1 = eb + gridDim.x;
+    const bool has1 = e1 < d.E;
+    for (int sl = sw; sl < kSW; sl += nsw)
+    for (int f0 = 0; f0 < nf; f0 += 128) {
+      const float4* w0 = reinterpret_cast<const float4*>(p.router_w + (size_t)e0 * d.H + sl * kw);
+      const float4* w1 = reinterpret_cast<const float4*>(p.router_w + (size_t)(has1 ? e1 : e0) * d.H +
+                                                         sl * kw);
+      float4 v0[4], v1[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int f = f0 + u * 32 + lane;
+        const bool ok = f < nf;
+        v0[u] = ok ? __ldg(w0 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v1[u] = ok && has1 ? __ldg(w1 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      for (int t0 = 0; t0 < d.T; t0 += 2) {
+        uint2 xv[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int t = min(t0 + j, d.T - 1);
+          const uint2* xr = reinterpret_cast<const uint2*>(p.x + (size_t)t * d.H + sl * kw);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int f = f0 + u * 32 + lane;
+            xv[j][u] = f < nf ? __ldg(xr + f) : make_uint2(0u, 0u);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int t = t0 + j;
+          if (t >= d.T) break;
+          float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint2 xw = xv[j][u];
+            const float x0 = __uint_as_float(xw.x << 16), x1 = __uint_as_float(xw.x & 0xffff0000u);
+            const float x2 = __uint_as_float(xw.y << 16), x3 = __uint_as_float(xw.y & 0xffff0000u);
+            a0 = fmaf(x0, v0[u].x, a0);
+            a0 = fmaf(x1, v0[u].y, a0);
+            a0 = fmaf(x2, v0[u].z, a0);
+            a0 = fmaf(x3, v0[u].w, a0);
+            a1 = fmaf(x0, v1[u].x, a1);
+            a1 = fmaf(x1, v1[u].y, a1);
+            a1 = fmaf(x2, v1[u].z, a1);
+            a1 = fmaf(x3, v1[u].w, a1);
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+            a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+          }
+          if (lane == 0) {
+            s.part[0][sl][t] = f0 == 0 ? a0 : s.part[0][sl][t] + a0;
+            s.part[1][sl][t] = f0 == 0 ? a1 : s.part[1][sl][t] + a1;
+          }
+        }
+      }
+    }
+    sbar(nsw);
+    if (tid < 2 * d.T) {
+      const int slot = tid / d.T, t = tid - slot * d.T;
+      if (slot == 0 || has1) {
+        float v = 0.f;
+        for (int w = 0; w < kSW; ++w) v += s.part[slot][w][t];
+        p.r.logits[(size_t)t * d.E + (slot ? e1 : e0)] = v;
+      }
+    }
+    sbar(nsw);
+  }
+}
+
 // Router warps: score this CTA's experts, wait for every CTA's logits, then
 // compute the whole routing in shared memory. Returns false on timeout.
 __device__ bool router_phase(Smem& s, const DecodeParams& p) {
   const Dims& d = p.d;
   const int tid = threadIdx.x - kRtr0 * 32, lane = tid & 31, warp = tid >> 5;
   for (int e = tid; e < d.E; e += kRW * 32) s.bias_s[e] = __ldg(p.router_bias + e);
-  const int kw = d.H / kRW;  // K slice of one warp
-  const int nf = kw / 4;
-  for (int eb = blockIdx.x; eb < d.E; eb += 2 * gridDim.x) {
-    const int e0 = eb, e1 = eb + gridDim.x;
-    const bool has1 = e1 < d.E;
-    const float4* w0 = reinterpret_cast<const float4*>(p.router_w + (size_t)e0 * d.H + warp * kw);
-    const float4* w1 = reinterpret_cast<const float4*>(p.router_w + (size_t)(has1 ? e1 : e0) * d.H +
-                                                       warp * kw);
-    for (int t = 0; t < d.T; ++t) {
-      const uint2* xr = reinterpret_cast<const uint2*>(p.x + (size_t)t * d.H + warp * kw);
-      float a0 = 0.f, a1 = 0.f;
-      for (int f0 = 0; f0 < nf; f0 += 128) {
-        float4 v0[4], v1[4];
-        uint2 xv[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int f = f0 + u * 32 + lane;
-          const bool ok = f < nf;
-          v0[u] = ok ? __ldg(w0 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
-          v1[u] = ok && has1 ? __ldg(w1 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
-          xv[u] = ok ? __ldg(xr + f) : make_uint2(0u, 0u);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float x0 = __uint_as_float(xv[u].x << 16), x1 = __uint_as_float(xv[u].x & 0xffff0000u);
-          const float x2 = __uint_as_float(xv[u].y << 16), x3 = __uint_as_float(xv[u].y & 0xffff0000u);
-          a0 = fmaf(x0, v0[u].x, a0);
-          a0 = fmaf(x1, v0[u].y, a0);
-          a0 = fmaf(x2, v0[u].z, a0);
-          a0 = fmaf(x3, v0[u].w, a0);
-          a1 = fmaf(x0, v1[u].x, a1);
-          a1 = fmaf(x1, v1[u].y, a1);
-          a1 = fmaf(x2, v1[u].z, a1);
-          a1 = fmaf(x3, v1[u].w, a1);
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        a0 += __shfl_xor_sync(0xffffffffu, a0, o);
-        a1 += __shfl_xor_sync(0xffffffffu, a1, o);
-      }
-      if (lane == 0) {
-        s.part[0][warp][t] = a0;
-        s.part[1][warp][t] = a1;
-      }
-    }
-    rbar();
-    if (tid < 2 * d.T) {
-      const int slot = tid / d.T, t = tid - slot * d.T;
-      if (slot == 0 || has1) {
-        float v = 0.f;
-        for (int w = 0; w < kRW; ++w) v += s.part[slot][w][t];
-        p.r.logits[(size_t)t * d.E + (slot ? e1 : e0)] = v;
-      }
-    }
-    rbar();
-  }
-  // publish this CTA's logits and wait for everybody's
+  score_experts(s, p, warp);
+  // publish this CTA's logits, then (off the logits' critical path) the
+  // interleaved x and group sums, then wait for everybody's logits
   if (tid == 0) {
     __threadfence();
     atomicAdd(&p.sync[0], 1u);
+  }
+  // this CTA's share of the tokens (t = b, b + G, ...): interleaved copy and
+  // per-group sums of x for the routed gate/up stages of every CTA; published on
+  // their own counter
+  {
+    const int h8 = d.H / 8;  // 16-byte chunks of a row; 16 per K group
+    for (int t = blockIdx.x; t < d.T; t += gridDim.x) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * d.H);
+      uint4* dst = reinterpret_cast<uint4*>(p.xi + (size_t)t * d.H);
+      for (int c0 = 0; c0 < h8; c0 += kRW * 32) {
+        const int cidx = c0 + tid;
+        float part = 0.f;
+        if (cidx < h8) {
+          const uint4 v = __ldg(src + cidx);
+          dst[(cidx & ~15) | chunk_t(cidx & 15)] = interleave8(v);
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            part += __uint_as_float(w4[q] << 16) + __uint_as_float(w4[q] & 0xffff0000u);
+        }
+        // the 16 chunks of a group sit in 16 consecutive lanes
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (cidx < h8 && (cidx & 15) == 0) p.xs[(size_t)t * p.xs_stride + (cidx >> 4)] = part;
+      }
+    }
+  }
+  rbar();
+  if (tid == 0) {
+    if ((int)blockIdx.x < d.T) {
+      __threadfence();
+      atomicAdd(&p.sync[1], 1u);
+    }
     s.flag = wait_counter(reinterpret_cast<const int*>(p.sync), (int)gridDim.x, p.r.err) ? 1 : 0;
   }
   for (int e = tid; e < kMaxExperts; e += kRW * 32) s.counts_s[e] = 0;
-  rbar();
+  rbar();  // thread 0 acquired the counter; the barrier orders everybody's reads after it
   if (!s.flag) return false;
-  (void)ld_acquire(reinterpret_cast<const int*>(p.sync));
 
-  // ---- the routing of every token, in shared memory
+  // ---- the routing of every token, in shared memory (the next token's logits
+  // are in flight while this one is ranked)
+  float lg[kPer], nx[kPer];
+  if (warp < d.T) load_logits(p.r.logits + (size_t)warp * d.E, d.E, lane, nx);
   for (int t = warp; t < d.T; t += kRW) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) lg[i] = nx[i];
+    if (t + kRW < d.T) load_logits(p.r.logits + (size_t)(t + kRW) * d.E, d.E, lane, nx);
     int id;
     float w;
-    warp_topk(p.r.logits + (size_t)t * d.E, s.bias_s, d.E, d.k, lane, &id, &w);
+    warp_topk(lg, s.bias_s, d.E, d.k, lane, &id, &w);
     if (lane < d.k) {
       if (id < 0 || id >= d.E) {
         atomicOr(p.r.err, kErrRange);
@@ -522,13 +685,27 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
   }
   rbar();
   const int n = d.T * d.k;
-  for (int i = tid; i < n; i += kRW * 32) {
-    const int ei = s.ids_s[i];
-    int rank = 0;
-    for (int j = 0; j < i; ++j) rank += (s.ids_s[j] == ei);
-    const int pos = s.offsets[ei] + rank;
-    s.perm_s[pos] = i / d.k;
-    s.inv_s[i] = pos;
+  if (warp == 0) {
+    // stable placement, 32 items at a time: rank among equal experts in the
+    // chunk by __match_any_sync, plus the expert's running count
+    for (int e = lane; e < d.E; e += 32) s.run_s[e] = s.offsets[e];
+    __syncwarp();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int c0 = 0; c0 < n; c0 += 32) {
+      const int i = c0 + lane;
+      const bool valid = i < n;
+      const int e = valid ? s.ids_s[i] : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(peers & lt);
+      if (valid) {
+        const int pos = s.run_s[e] + rank;
+        s.perm_s[pos] = i / d.k;
+        s.inv_s[i] = pos;
+      }
+      __syncwarp();
+      if (valid && rank == 0) s.run_s[e] += __popc(peers);
+      __syncwarp();
+    }
   }
   rbar();
   if (tid == 0) mbar_arrive(&s.route_ready);
@@ -567,13 +744,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>(smem_raw);
+  uint8_t* const stage_base = smem_raw + kStageOff;
+  const int nst = p.nst, sb = p.stage_bytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Dims& d = p.d;
   unsigned* err = p.r.err;
   const bool scale_tma = p.scale_tma != 0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kS; ++i) {
+    for (int i = 0; i < p.nst; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], kCW);
       mbar_init(&s.desc_ready[i], 1);
@@ -628,8 +807,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           Desc& ds = s.desc[stage];
+          const bool pre = !t.shared && !t.down;
           ds.flags = (g0 == 0 ? kFirst : 0) | (g0 + 8 >= t.ngroups ? kLast : 0) |
-                     (t.shared ? kShared : 0) | (t.down ? kDown : 0);
+                     (t.shared ? kShared : 0) | (t.down ? kDown : 0) | (pre ? kPre : 0);
           ds.g0 = g0;
           ds.gcnt = gcnt;
           ds.ngroups = t.ngroups;
@@ -641,8 +821,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ds.cnt = t.e * kMaxPass + t.pass;
           // the activation warp copies nr rows into the stage; a TMA box always
           // delivers its full size (out-of-range parts are zero-filled)
-          mbar_arrive_expect_tx(&s.full[stage], kWB + (scale_tma ? kSB : 0) + t.nr * gcnt * 256);
-          uint8_t* st = s.stage[stage];
+          mbar_arrive_expect_tx(&s.full[stage],
+                                kWB + (scale_tma ? kSB : 0) + t.nr * (gcnt * 256 + (pre ? 32 : 0)));
+          uint8_t* st = stage_base + (size_t)stage * sb;
           tma_2d(smem_u32(st), tm, &s.full[stage], g0 * 16, t.rowA0);
           tma_2d(smem_u32(st + kWB / 2), tm, &s.full[stage], g0 * 16, t.rowA1);
           if (scale_tma) {
@@ -650,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_2d(smem_u32(st + kWB + kSB / 2), ts, &s.full[stage], g0, t.rowA1);
           }
           mbar_arrive(&s.desc_ready[stage]);
-          if (++stage == kS) {
+          if (++stage == nst) {
             stage = 0;
             phase ^= 1u;
           }
@@ -669,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- activation rows
     int stage = 0;
     uint32_t phase = 0;
-    bool routed_known = false;
+    bool routed_known = false, pre_ready = false;
     // poll every active (expert, pass) gate/up counter once (lanes in parallel)
     // and record the finished ones; returns true when pair `want` is finished
     auto poll_pairs = [&](int want) -> bool {
@@ -721,17 +902,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         fence_proxy_async();
       }
+      if ((ds.flags & kPre) && !pre_ready) {
+        // interleaved x and group sums come from other CTAs' generic stores,
+        // published on their own counter by the CTAs that own a token
+        int ok = 1;
+        if (lane == 0)
+          ok = wait_counter(reinterpret_cast<const int*>(p.sync + 1), min(d.T, (int)gridDim.x), err) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        __syncwarp();
+        fence_proxy_async();
+        pre_ready = true;
+      }
       if (lane < ds.nr) {
         const int r = ds.r0 + lane;
+        const uint32_t slot = smem_u32(stage_base + (size_t)stage * sb + kXO + lane * kXS);
         const uint16_t* src;
-        if (!down)
-          src = p.x + (size_t)((ds.flags & kShared) ? r - d.T * d.k : s.perm_s[r]) * d.H;
-        else
+        if (ds.flags & kPre) {
+          const int tok = s.perm_s[r];
+          src = p.xi + (size_t)tok * d.H;
+          bulk_copy(slot + kXSumO, p.xs + (size_t)tok * p.xs_stride + ds.g0, 32, &s.full[stage]);
+        } else if (!down) {
+          src = p.x + (size_t)((ds.flags & kShared) ? r - d.T * d.k : r) * d.H;
+        } else {
           src = p.h + (size_t)r * p.hstride;
-        bulk_copy(smem_u32(s.stage[stage] + kXO + lane * kXS), src + ds.g0 * kGroup, ds.gcnt * 256,
-                  &s.full[stage]);
+        }
+        bulk_copy(slot, src + ds.g0 * kGroup, ds.gcnt * 256, &s.full[stage]);
       }
-      if (++stage == kS) {
+      if (++stage == nst) {
         stage = 0;
         phase ^= 1u;
       }
@@ -740,10 +937,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- consumers
     const int g = lane >> 2, c = lane & 3;
     const int gw = warp & 7, tl = warp >> 3;
-    const uint32_t stage0 = smem_u32(s.stage[0]);
+    const uint32_t stage0 = smem_u32(stage_base);
     const uint32_t w_off = tl * (kWB / 2) + g * 512 + gw * 64 + c * 16;
     const uint32_t s_off = kWB + tl * (kSB / 2) + g * 16 + gw * 2;
-    const uint32_t x_off = kXO + g * kXS + gw * 256 + c * 64;
+    const uint32_t x_off = kXO + g * kXS + gw * 256 + c * 64;  // natural chunk order
+    const uint32_t xt_off = kXO + g * kXS + gw * 256 + c * 16;  // transposed (xi, h)
     int stage = 0;
     uint32_t phase = 0;
     int tseq = 0;  // tasks finished (the same sequence for all consumer warps)
@@ -754,7 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ds.flags & kEnd) break;
       if (ds.flags & kFirst) acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
       if (gw < ds.gcnt) {
-        const uint32_t st = stage0 + stage * kStageB;
+        const uint32_t st = stage0 + stage * sb;
         const uint4 wA = lds128(st + w_off), wB = lds128(st + w_off + 8 * 512);
         float s0, s1;
         if (scale_tma) {
@@ -767,12 +965,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           s0 = bf16_bits_to_f32(__ldg(scl + (size_t)row * ds.ngroups + ds.g0 + gw));
           s1 = bf16_bits_to_f32(__ldg(scl + (size_t)(row + 8) * ds.ngroups + ds.g0 + gw));
         }
+        const bool pre = (ds.flags & kPre) != 0;
         uint4 b[4];
         if (g < ds.nr) {
+          if (ds.flags & (kDown | kPre)) {
+            // chunk 4c + m of the group sits at 4m + c: the 4 lanes of a row
+            // read 64 contiguous bytes per step (no bank conflicts)
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            b[m] = lds128(st + x_off + m * 16);
-            if (!(ds.flags & kDown)) b[m] = interleave8(b[m]);
+            for (int m = 0; m < 4; ++m) b[m] = lds128(st + xt_off + m * 64);
+          } else {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) b[m] = interleave8(lds128(st + x_off + m * 16));
           }
         } else {
 #pragma unroll
@@ -780,24 +983,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // 8 MMA steps in 4 independent chains
         float t4[4][4] = {};
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const uint32_t ra = word_of(wA, m), rb = word_of(wB, m);
-          uint32_t a[4];
-          a[0] = int4_pair_to_bf16x2<0>(ra);
-          a[1] = int4_pair_to_bf16x2<0>(rb);
-          a[2] = int4_pair_to_bf16x2<1>(ra);
-          a[3] = int4_pair_to_bf16x2<1>(rb);
-          mma_bf16_16816(t4[(2 * m) & 3], a, b[m].x, b[m].y, t4[(2 * m) & 3]);
-          a[0] = int4_pair_to_bf16x2<2>(ra);
-          a[1] = int4_pair_to_bf16x2<2>(rb);
-          a[2] = int4_pair_to_bf16x2<3>(ra);
-          a[3] = int4_pair_to_bf16x2<3>(rb);
-          mma_bf16_16816(t4[(2 * m + 1) & 3], a, b[m].z, b[m].w, t4[(2 * m + 1) & 3]);
-        }
+        if (pre)
+          stage_mma<true>(wA, wB, b, t4);
+        else
+          stage_mma<false>(wA, wB, b, t4);
         float tmp[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) tmp[i] = (t4[0][i] + t4[1][i]) + (t4[2][i] + t4[3][i]);
+        if (pre) {
+          // the weights were 136 + q: take 136 * sum(x) of tokens 2c, 2c + 1 off
+          const float xs0 = 2 * c < ds.nr ? lds_f32(st + kXO + 2 * c * kXS + kXSumO + gw * 4) : 0.f;
+          const float xs1 =
+              2 * c + 1 < ds.nr ? lds_f32(st + kXO + (2 * c + 1) * kXS + kXSumO + gw * 4) : 0.f;
+          tmp[0] = fmaf(-136.f, xs0, tmp[0]);
+          tmp[1] = fmaf(-136.f, xs1, tmp[1]);
+          tmp[2] = fmaf(-136.f, xs0, tmp[2]);
+          tmp[3] = fmaf(-136.f, xs1, tmp[3]);
+        }
         acc[0] = fmaf(s0, tmp[0], acc[0]);
         acc[1] = fmaf(s0, tmp[1], acc[1]);
         acc[2] = fmaf(s1, tmp[2], acc[2]);
@@ -805,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.empty[stage]);
-      if (++stage == kS) {
+      if (++stage == nst) {
         stage = 0;
         phase ^= 1u;
       }
@@ -834,6 +1036,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     router_phase(s, p);
   } else {
     // ---------------------------------------------------------------- epilogue
+    if (scoring_warps(d) > kRW) score_experts(s, p, kRW + (warp - kEpi0));
     const int b = warp - kEpi0;  // this warp's slot
     const int g = lane >> 2, c = lane & 3;
     int routed_down = -1;
@@ -867,7 +1070,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t orow = (size_t)(ds.r0 + tok);
         if (!down) {
           const int n = ds.tile * kTile1 + row;
-          const int pos = (n & ~7) | ((n & 3) << 1) | ((n >> 2) & 1);
+          // interleaved within 8, 16-byte chunks transposed within the K group
+          const int pos = (n & ~127) | (chunk_t((n >> 3) & 15) << 3) | ((n & 3) << 1) | ((n >> 2) & 1);
           p.h[orow * p.hstride + pos] = f32_to_bf16_bits(silu(f0[q]) * f1[q]);
         } else {
           float* yr = p.y + orow * d.H + ds.tile * kTile2;
@@ -924,7 +1128,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __threadfence();
     for (int i = threadIdx.x; i < (d.E + 1) * kMaxPass; i += blockDim.x) p.done1[i] = 0;
     for (int i = threadIdx.x; i < d.H / kTile2; i += blockDim.x) p.tile_cnt[i] = 0;
-    if (threadIdx.x == 0) p.sync[0] = 0u;
+    if (threadIdx.x == 0) {
+      p.sync[0] = 0u;
+      p.sync[1] = 0u;
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
       __threadfence();
@@ -935,19 +1142,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+// Ring geometry for a batch of T tokens: as many stages as fit (at most
+// kMaxS), each holding min(T, kR) activation rows.
+static void ring_of(int T, int* nst, int* stage_bytes) {
+  const int rows = T < kR ? (T < 1 ? 1 : T) : kR;
+  *stage_bytes = (kXO + rows * kXS + 1023) / 1024 * 1024;
+  const int n = (kSmemMax - kStageOff) / *stage_bytes;
+  *nst = n < kMaxS ? n : kMaxS;
+}
+
 cudaError_t decode_setup(int* ctas_per_sm) {
   cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)sizeof(Smem));
+                                       kSmemMax);
   if (e != cudaSuccess) return e;
+  int nst, sb;
+  ring_of(kSmallT, &nst, &sb);
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_kernel, kThreads,
-                                                       sizeof(Smem));
+                                                       kStageOff + nst * sb);
 }
+
+int decode_xs_stride(int H) { return (H / kGroup + 7) / 8 * 8; }
 
 size_t decode_counter_ints(int E, int H) { return (size_t)(E + 1) * kMaxPass + H / kTile2 + 4; }
 
 cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& w, const uint16_t* x,
-                          uint16_t* h, int hstride, float* y, uint16_t* out, int* counters, int grid,
-                          cudaStream_t s, LaunchLog& log) {
+                          uint16_t* xi, float* xs, uint16_t* h, int hstride, float* y, uint16_t* out,
+                          int* counters, int grid, cudaStream_t s, LaunchLog& log) {
   DecodeParams p{};
   p.d = d;
   p.r = r;
@@ -958,6 +1178,9 @@ cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& 
   p.s13_shared = w.s13_shared;
   p.s2_routed = w.s2_routed;
   p.s2_shared = w.s2_shared;
+  p.xi = xi;
+  p.xs = xs;
+  p.xs_stride = decode_xs_stride(d.H);
   p.h = h;
   p.hstride = hstride;
   p.y = y;
@@ -966,11 +1189,12 @@ cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& 
   p.tile_cnt = counters + (size_t)(d.E + 1) * kMaxPass;
   p.sync = reinterpret_cast<unsigned*>(p.tile_cnt + d.H / kTile2);
   p.scale_tma = w.scale_tma;
+  ring_of(d.T, &p.nst, &p.stage_bytes);
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = sizeof(Smem);
+  cfg.dynamicSmemBytes = kStageOff + p.nst * p.stage_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;

@@ -82,9 +82,12 @@ struct DecodeWeights {
 };
 cudaError_t decode_setup(int* ctas_per_sm);
 size_t decode_counter_ints(int E, int H);
+// xi: [T, H] bf16 scratch (x interleaved), xs: [T, decode_xs_stride(H)] fp32
+// scratch (x summed over each K group), both written by the kernel itself.
+int decode_xs_stride(int H);
 cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& w, const uint16_t* x,
-                          uint16_t* h, int hstride, float* y, uint16_t* out, int* counters, int grid,
-                          cudaStream_t s, LaunchLog& log);
+                          uint16_t* xi, float* xs, uint16_t* h, int hstride, float* y, uint16_t* out,
+                          int* counters, int grid, cudaStream_t s, LaunchLog& log);
 
 // Tensor-core (tcgen05) expert GEMMs for large batches.
 struct TcWeights {

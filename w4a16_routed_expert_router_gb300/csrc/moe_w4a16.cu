@@ -45,6 +45,7 @@ struct moe_w4a16_handle {
   CUtensorMap xmap, hmap;
   // tensor-core router: bf16 planes of router_w and the view of this call's x
   uint16_t* planes = nullptr;
+  float* xs = nullptr;          // decode: x summed per K group (x interleaved lives in xperm)
   CUtensorMap wmap_router, xmap_router;
   const void* xmap_key = nullptr;
   int xmap_rows = 0;
@@ -133,6 +134,7 @@ Layout plan(const moe_w4a16_config& c) {
       (E + 2) * 4,           // 22 task3
       (E + 2) * 4,           // 23 task4
       3 * E * H * 2,         // 24 router planes
+      Tm * decode_xs_stride(c.hidden) * 4,  // 25 decode: x summed per K group
   };
   Layout L;
   size_t o = 0;
@@ -379,6 +381,7 @@ int moe_w4a16_create(const moe_w4a16_config* cfg, int device, moe_w4a16_handle**
   r.task3 = reinterpret_cast<int*>(b + L.off[22]);
   r.task4 = reinterpret_cast<int*>(b + L.off[23]);
   h->planes = reinterpret_cast<uint16_t*>(b + L.off[24]);
+  h->xs = reinterpret_cast<float*>(b + L.off[25]);
   if (h->tc_ok) {
     const long long rows = (long long)cfg->max_tokens * (cfg->top_k + 1);
     if ((st = encode_act_map_tc(&h->xmap, r.xperm, cfg->hidden, rows)) != MOE_W4A16_OK ||
@@ -501,8 +504,8 @@ int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t T, const m
     dw.ts2r = g2.ts_routed;
     dw.ts2s = g2.ts_shared;
     dw.scale_tma = scale_tma;
-    if ((e = launch_decode(d, h->r, dw, x, h->h, h->hstride, h->y, out, h->counters,
-                           h->decode_grid, s, h->log)) != cudaSuccess)
+    if ((e = launch_decode(d, h->r, dw, x, h->r.xperm, h->xs, h->h, h->hstride, h->y, out,
+                           h->counters, h->decode_grid, s, h->log)) != cudaSuccess)
       return cuda_status(e);
     h->last_T = T;
     return MOE_W4A16_OK;
@@ -665,7 +668,7 @@ NoAllocDevice g_noalloc[kMaxDevices];
 std::mutex g_noalloc_mu;
 
 struct NoAllocLayout {
-  size_t off[16];
+  size_t off[24];
   size_t total;
 };
 
@@ -689,6 +692,8 @@ NoAllocLayout noalloc_plan(const moe_w4a16_config& c, int T) {
       decode_counter_ints(c.num_experts, c.hidden) * 4,  // 12 counters
       rows * hstride * 2,                                // 13 h
       rows * H * 4,                                      // 14 y
+      Tz * H * 2,                                        // 15 x interleaved
+      Tz * decode_xs_stride(c.hidden) * 4,               // 16 x group sums
   };
   NoAllocLayout L;
   size_t o = 0;
@@ -772,6 +777,8 @@ extern "C" int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint
   int* counters = reinterpret_cast<int*>(b + L.off[12]);
   uint16_t* hbuf = reinterpret_cast<uint16_t*>(b + L.off[13]);
   float* ybuf = reinterpret_cast<float*>(b + L.off[14]);
+  uint16_t* xibuf = reinterpret_cast<uint16_t*>(b + L.off[15]);
+  float* xsbuf = reinterpret_cast<float*>(b + L.off[16]);
   const int hstride = c.inter > c.shared_inter ? c.inter : c.shared_inter;
 
   // tensor maps, encoded on the host for this call
@@ -822,5 +829,6 @@ extern "C" int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint
   if ((st = cuda_status(cudaMemsetAsync(r.err, 0, 4, s))) != MOE_W4A16_OK) return st;
   Dims d{T, c.hidden, c.num_experts, c.top_k, c.inter, c.shared_inter};
   LaunchLog log;
-  return cuda_status(launch_decode(d, r, dw, x, hbuf, hstride, ybuf, out, counters, nd.grid, s, log));
+  return cuda_status(
+      launch_decode(d, r, dw, x, xibuf, xsbuf, hbuf, hstride, ybuf, out, counters, nd.grid, s, log));
 }

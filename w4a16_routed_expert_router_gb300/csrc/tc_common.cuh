@@ -26,8 +26,8 @@ __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, unsigned* 
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if ((i & 15u) == 0) {
       if (aborted(err)) return false;
       if (global_ns() - t0 > kWaitLimitNs) {
         atomicOr(err, kErrTimeout);
