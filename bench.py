@@ -310,10 +310,13 @@ def run_ours(args, shape):
     def flush_l2():
         torch.sum(flush, dim=0, out=flush_out)
 
+    path_flags = {"auto": 0, "tc": moe.MOE_W4A16_FLAG_FORCE_TC,
+                  "gemv": moe.MOE_W4A16_FLAG_FORCE_GEMV}[args.expert_path]
     obj = moe.MoeLayer(shape.hidden, shape.experts, shape.top_k, shape.inter,
-                       shape.shared_inter, T, tensors)
+                       shape.shared_inter, T, tensors, flags=path_flags)
     prof = moe.MoeLayer(shape.hidden, shape.experts, shape.top_k, shape.inter,
-                        shape.shared_inter, T, tensors, flags=moe.MOE_W4A16_FLAG_PROFILE)
+                        shape.shared_inter, T, tensors,
+                        flags=path_flags | moe.MOE_W4A16_FLAG_PROFILE)
     stream = torch.cuda.Stream(device=dev)
     xin = torch.empty_like(xs[0])
 
@@ -418,7 +421,8 @@ def run_ours(args, shape):
                        "experts": shape.experts, "top_k": shape.top_k, "inter": shape.inter,
                        "shared_inter": shape.shared_inter, "weights": "int4 g128 symmetric",
                        "l2": "flushed before every step (512 MB read, untimed)",
-                       "graph": "one forward per CUDA-graph replay", "parallelism": "replicas"},
+                       "graph": "one forward per CUDA-graph replay", "parallelism": "replicas",
+                       "expert_path": args.expert_path},
             "weight_stream_gbs": work["weight_bytes"] / (ms_per_step / 1000.0) / 1e9,
             "layer_roofline_frac": layer_roof_s / (ms_per_step / 1000.0),
             "experts_hit": work["hit"],
@@ -449,6 +453,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="decode1", choices=ms.CONFIG_ORDER)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--expert-path", default="auto", choices=["auto", "tc", "gemv"],
+                    help="expert kernels: the library's choice, tensor-core, or split-K GEMV")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
