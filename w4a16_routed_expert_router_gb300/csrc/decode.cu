@@ -25,10 +25,10 @@
 //    scan, stable permutation, task lists). Computing it redundantly per CTA
 //    keeps the critical path at two global round trips, and it overlaps the
 //    shared expert's work, which needs no routing.
-//  * 16 consumer warps stream stages from the start: warp w takes K-group
-//    (w % 8) of tile (w / 8); exact INT4 -> bf16 in registers, mma.sync
-//    m16n8k16 with weights as A and up to 8 rows as B, group scales applied
-//    in fp32. At the end of a task each warp drops its partial sums into a
+//  * 8 consumer warps stream stages from the start: warp w takes K-group w
+//    of both tiles (the activation fragments serve both; 8 independent MMA
+//    chains per warp); exact INT4 -> bf16 in registers, mma.sync m16n8k16
+//    with weights as A and up to 8 rows as B, group scales applied in fp32. At the end of a task each warp drops its partial sums into a
 //    slot and moves on. Routed gate/up stages skip two steps: their x rows
 //    come pre-interleaved, and the weights stay 136 + q (one op per code
 //    pair) with 136 * sum(x over the group) taken off each group's dot
@@ -65,7 +65,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kCW = 16;                      // consumer warps
+constexpr int kCW = 8;                       // consumer warps (one per K group, both tiles)
 constexpr int kEW = 4;                       // epilogue warps (= slots)
 constexpr int kRW = 4;                       // router warps
 constexpr int kProd = kCW;                   // weight producer warp index
@@ -93,7 +93,7 @@ struct Desc {
 };
 
 struct Smem {
-  float4 red[kEW][kCW * 32];            // task-end partial sums, one slot per epilogue warp
+  float4 red[kEW][16 * 32];             // task-end partial sums (K group x tile), one slot per epilogue warp
   float part[2][kSW][kSmallT];          // router: per-warp partial logits of 2 experts
   float bias_s[kMaxExperts];
   Desc slot_desc[kEW];
@@ -936,34 +936,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kCW) {
     // ---------------------------------------------------------------- consumers
     const int g = lane >> 2, c = lane & 3;
-    const int gw = warp & 7, tl = warp >> 3;
+    const int gw = warp;  // K group of the stage; both 16-row tiles
     const uint32_t stage0 = smem_u32(stage_base);
-    const uint32_t w_off = tl * (kWB / 2) + g * 512 + gw * 64 + c * 16;
-    const uint32_t s_off = kWB + tl * (kSB / 2) + g * 16 + gw * 2;
+    const uint32_t w_off = g * 512 + gw * 64 + c * 16;
+    const uint32_t s_off = kWB + g * 16 + gw * 2;
     const uint32_t x_off = kXO + g * kXS + gw * 256 + c * 64;  // natural chunk order
     const uint32_t xt_off = kXO + g * kXS + gw * 256 + c * 16;  // transposed (xi, h)
     int stage = 0;
     uint32_t phase = 0;
     int tseq = 0;  // tasks finished (the same sequence for all consumer warps)
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[2][4] = {};
     for (;;) {
       if (!dwait(&s.full[stage], phase, err)) break;
       const Desc ds = s.desc[stage];
       if (ds.flags & kEnd) break;
-      if (ds.flags & kFirst) acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+      if (ds.flags & kFirst) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[0][i] = acc[1][i] = 0.f;
+      }
       if (gw < ds.gcnt) {
         const uint32_t st = stage0 + stage * sb;
-        const uint4 wA = lds128(st + w_off), wB = lds128(st + w_off + 8 * 512);
-        float s0, s1;
-        if (scale_tma) {
-          s0 = bf16_bits_to_f32(lds16(st + s_off));
-          s1 = bf16_bits_to_f32(lds16(st + s_off + 8 * 16));
-        } else {
-          const uint16_t* scl = (ds.flags & kDown) ? ((ds.flags & kShared) ? p.s2_shared : p.s2_routed)
-                                                   : ((ds.flags & kShared) ? p.s13_shared : p.s13_routed);
-          const int row = (tl ? ds.rowA1 : ds.rowA0) + g;
-          s0 = bf16_bits_to_f32(__ldg(scl + (size_t)row * ds.ngroups + ds.g0 + gw));
-          s1 = bf16_bits_to_f32(__ldg(scl + (size_t)(row + 8) * ds.ngroups + ds.g0 + gw));
+        uint4 wA[2], wB[2];
+        float sc[2][2];  // [tile][row g / g + 8]
+#pragma unroll
+        for (int tl = 0; tl < 2; ++tl) {
+          wA[tl] = lds128(st + tl * (kWB / 2) + w_off);
+          wB[tl] = lds128(st + tl * (kWB / 2) + w_off + 8 * 512);
+          if (scale_tma) {
+            sc[tl][0] = bf16_bits_to_f32(lds16(st + tl * (kSB / 2) + s_off));
+            sc[tl][1] = bf16_bits_to_f32(lds16(st + tl * (kSB / 2) + s_off + 8 * 16));
+          } else {
+            const uint16_t* scl = (ds.flags & kDown) ? ((ds.flags & kShared) ? p.s2_shared : p.s2_routed)
+                                                     : ((ds.flags & kShared) ? p.s13_shared : p.s13_routed);
+            const int row = (tl ? ds.rowA1 : ds.rowA0) + g;
+            sc[tl][0] = bf16_bits_to_f32(__ldg(scl + (size_t)row * ds.ngroups + ds.g0 + gw));
+            sc[tl][1] = bf16_bits_to_f32(__ldg(scl + (size_t)(row + 8) * ds.ngroups + ds.g0 + gw));
+          }
         }
         const bool pre = (ds.flags & kPre) != 0;
         uint4 b[4];
@@ -981,29 +989,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int m = 0; m < 4; ++m) b[m] = make_uint4(0u, 0u, 0u, 0u);
         }
-        // 8 MMA steps in 4 independent chains
-        float t4[4][4] = {};
-        if (pre)
-          stage_mma<true>(wA, wB, b, t4);
-        else
-          stage_mma<false>(wA, wB, b, t4);
-        float tmp[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) tmp[i] = (t4[0][i] + t4[1][i]) + (t4[2][i] + t4[3][i]);
+        // 2 tiles x 8 MMA steps in 8 independent chains (the x fragments are
+        // shared by both tiles)
+        float t4[2][4][4] = {};
+        if (pre) {
+          stage_mma<true>(wA[0], wB[0], b, t4[0]);
+          stage_mma<true>(wA[1], wB[1], b, t4[1]);
+        } else {
+          stage_mma<false>(wA[0], wB[0], b, t4[0]);
+          stage_mma<false>(wA[1], wB[1], b, t4[1]);
+        }
+        float xs0 = 0.f, xs1 = 0.f;
         if (pre) {
           // the weights were 136 + q: take 136 * sum(x) of tokens 2c, 2c + 1 off
-          const float xs0 = 2 * c < ds.nr ? lds_f32(st + kXO + 2 * c * kXS + kXSumO + gw * 4) : 0.f;
-          const float xs1 =
-              2 * c + 1 < ds.nr ? lds_f32(st + kXO + (2 * c + 1) * kXS + kXSumO + gw * 4) : 0.f;
-          tmp[0] = fmaf(-136.f, xs0, tmp[0]);
-          tmp[1] = fmaf(-136.f, xs1, tmp[1]);
-          tmp[2] = fmaf(-136.f, xs0, tmp[2]);
-          tmp[3] = fmaf(-136.f, xs1, tmp[3]);
+          if (2 * c < ds.nr) xs0 = lds_f32(st + kXO + 2 * c * kXS + kXSumO + gw * 4);
+          if (2 * c + 1 < ds.nr) xs1 = lds_f32(st + kXO + (2 * c + 1) * kXS + kXSumO + gw * 4);
         }
-        acc[0] = fmaf(s0, tmp[0], acc[0]);
-        acc[1] = fmaf(s0, tmp[1], acc[1]);
-        acc[2] = fmaf(s1, tmp[2], acc[2]);
-        acc[3] = fmaf(s1, tmp[3], acc[3]);
+#pragma unroll
+        for (int tl = 0; tl < 2; ++tl) {
+          float tmp[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            tmp[i] = (t4[tl][0][i] + t4[tl][1][i]) + (t4[tl][2][i] + t4[tl][3][i]);
+          if (pre) {
+            tmp[0] = fmaf(-136.f, xs0, tmp[0]);
+            tmp[1] = fmaf(-136.f, xs1, tmp[1]);
+            tmp[2] = fmaf(-136.f, xs0, tmp[2]);
+            tmp[3] = fmaf(-136.f, xs1, tmp[3]);
+          }
+          acc[tl][0] = fmaf(sc[tl][0], tmp[0], acc[tl][0]);
+          acc[tl][1] = fmaf(sc[tl][0], tmp[1], acc[tl][1]);
+          acc[tl][2] = fmaf(sc[tl][1], tmp[2], acc[tl][2]);
+          acc[tl][3] = fmaf(sc[tl][1], tmp[3], acc[tl][3]);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.empty[stage]);
@@ -1016,7 +1034,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = tseq % kEW;
       const uint32_t use = (uint32_t)(tseq / kEW);
       if (!dwait(&s.slot_free[b], (use & 1u) ^ 1u, err)) break;
-      s.red[b][warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      s.red[b][warp * 32 + lane] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+      s.red[b][(8 + warp) * 32 + lane] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
       if (warp == 0 && lane == 0) s.slot_desc[b] = ds;
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.slot_full[b]);
