@@ -176,6 +176,18 @@ int moe_w4a16_last_launches(moe_w4a16_handle* h, int32_t* count, const char** na
 int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint16_t* x, int32_t num_tokens,
                               const moe_w4a16_weights* w, uint16_t* out, void* stream);
 
+/* Pack signed 4-bit weights into the storage format of w13_q / w2_q.
+ *
+ * q: host int8 [rows, K], row-major, every value in [-8, 7]; out: host
+ * uint32 [rows, K/8]. Element kk of a row goes to word kk/8, code kk%8 (bits
+ * 4*(kk%8) .. +3) as u = q + 8, which is the layout the header describes for
+ * the packed tensors ("canada-quant/DeepSeek-V4-Flash-W4A16-FP8-MTP", table
+ * "Component precisions": INT4, symmetric, group 128). Synchronous, no
+ * device work; the caller owns both buffers. Returns
+ * MOE_W4A16_ERR_INVALID_ARG for null pointers, rows < 0, K not a positive
+ * multiple of 8, or a value outside [-8, 7]; nothing is written then. */
+int moe_w4a16_pack_int4(const int8_t* q, int64_t rows, int64_t K, uint32_t* out);
+
 /* Static description of a status code. */
 const char* moe_w4a16_status_string(int status);
 

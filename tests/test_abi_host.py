@@ -5,9 +5,11 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import w4a16_routed_expert_router_gb300 as moe
+from oracle import moe_oracle as mo
 from w4a16_routed_expert_router_gb300 import _build
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
@@ -22,7 +24,7 @@ def L():
 
 def _declared():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"\b(moe_w4a16_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(moe_w4a16_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_binding_names():
@@ -104,3 +106,31 @@ def test_create_without_a_gpu_reports_no_device(L):
     h = ctypes.c_void_p()
     assert L.moe_w4a16_create(ctypes.byref(_cfg()), 0, ctypes.byref(h)) == \
         moe.MOE_W4A16_ERR_NO_DEVICE
+
+
+# ------------------------------------------------------------------ packing
+def test_pack_int4_matches_the_documented_patterns():
+    # code j of a word holds element 8w + j as u = q + 8
+    q = np.array([[-8, -7, -6, -5, -4, -3, -2, -1, 0, 1, 2, 3, 4, 5, 6, 7],
+                  [0] * 16], dtype=np.int8)
+    words = moe.moe_w4a16_pack_int4(q)
+    assert words.dtype == np.uint32 and words.shape == (2, 2)
+    assert words[0].tolist() == [0x76543210, 0xFEDCBA98]
+    assert words[1].tolist() == [0x88888888, 0x88888888]
+
+
+def test_pack_int4_inverts_the_oracle_unpack():
+    rng = np.random.default_rng(7)
+    q = rng.integers(-8, 8, size=(33, 256), dtype=np.int8)
+    words = moe.moe_w4a16_pack_int4(q)
+    np.testing.assert_array_equal(mo.unpack_int4(words), q.astype(np.int64))
+
+
+def test_pack_int4_rejects_bad_input_without_writing():
+    q = np.zeros((2, 16), dtype=np.int8)
+    q[1, 3] = 8
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_w4a16_pack_int4(q)
+    assert ei.value.status == moe.MOE_W4A16_ERR_INVALID_ARG
+    with pytest.raises(moe.MoeError):
+        moe.moe_w4a16_pack_int4(np.zeros((2, 12), dtype=np.int8))

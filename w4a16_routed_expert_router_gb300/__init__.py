@@ -38,6 +38,7 @@ EXPORTS = (
     "moe_w4a16_last_launches",
     "moe_w4a16_status_string",
     "moe_w4a16_forward_noalloc",
+    "moe_w4a16_pack_int4",
 )
 MOE_W4A16_NOALLOC_MAX_TOKENS = 16
 
@@ -94,6 +95,7 @@ def lib() -> ctypes.CDLL:
                                          ctypes.POINTER(ctypes.c_float), i32], ctypes.c_int),
             "moe_w4a16_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "moe_w4a16_forward_noalloc": ([cfgp, vp, i32, wp, vp, vp], ctypes.c_int),
+            "moe_w4a16_pack_int4": ([vp, ctypes.c_int64, ctypes.c_int64, vp], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -153,6 +155,20 @@ def moe_w4a16_forward_noalloc(cfg: moe_w4a16_config, x_ptr: int, num_tokens: int
     _check(lib().moe_w4a16_forward_noalloc(ctypes.byref(cfg), x_ptr, num_tokens,
                                            ctypes.byref(weights), out_ptr, stream),
            "moe_w4a16_forward_noalloc")
+
+
+def moe_w4a16_pack_int4(q):
+    """Pack signed 4-bit values (int8 numpy [rows, K], values in [-8, 7]) into
+    the uint32 [rows, K/8] layout of the packed weight tensors (host only)."""
+    import numpy as np
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    if q.ndim != 2:
+        raise ValueError("q must be 2-D [rows, K]")
+    rows, K = q.shape
+    out = np.empty((rows, max(K // 8, 0)), dtype=np.uint32)
+    _check(lib().moe_w4a16_pack_int4(q.ctypes.data, rows, K, out.ctypes.data),
+           "moe_w4a16_pack_int4")
+    return out
 
 
 def moe_w4a16_get_routing(handle, ids=0, wts=0, offsets=0, perm=0, inv=0, stream=0) -> None:

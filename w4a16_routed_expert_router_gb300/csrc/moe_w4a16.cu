@@ -288,6 +288,19 @@ const char* moe_w4a16_status_string(int s) {
   }
 }
 
+int moe_w4a16_pack_int4(const int8_t* q, int64_t rows, int64_t K, uint32_t* out) {
+  if (!q || !out || rows < 0 || K <= 0 || K % 8) return MOE_W4A16_ERR_INVALID_ARG;
+  const int64_t n = rows * K;
+  for (int64_t i = 0; i < n; ++i)
+    if (q[i] < -8 || q[i] > 7) return MOE_W4A16_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < n; i += 8) {
+    uint32_t w = 0;
+    for (int j = 0; j < 8; ++j) w |= (uint32_t)(q[i + j] + 8) << (4 * j);
+    out[i / 8] = w;
+  }
+  return MOE_W4A16_OK;
+}
+
 int moe_w4a16_workspace_bytes(const moe_w4a16_config* cfg, size_t* bytes) {
   const int st = validate_config(cfg);
   if (st != MOE_W4A16_OK) return st;
