@@ -26,8 +26,8 @@
 //    keeps the critical path at two global round trips, and it overlaps the
 //    shared expert's work, which needs no routing.
 //  * 8 consumer warps stream stages from the start: warp w takes K-group w
-//    of both tiles (the activation fragments serve both; 8 independent MMA
-//    chains per warp); exact INT4 -> bf16 in registers, mma.sync m16n8k16
+//    of both tiles (the activation fragments serve both; one MMA chain per
+//    tile); exact INT4 -> bf16 in registers, mma.sync m16n8k16
 //    with weights as A and up to 8 rows as B, group scales applied in fp32. At the end of a task each warp drops its partial sums into a
 //    slot and moves on. Routed gate/up stages skip two steps: their x rows
 //    come pre-interleaved, and the weights stay 136 + q (one op per code
@@ -252,11 +252,12 @@ __device__ __forceinline__ float lds_f32(uint32_t addr) {
   return v;
 }
 
-// The 8 MMA steps of one K group of one stage (4 independent chains). OFFSET:
-// the A operand holds 136 + q (the caller corrects with the x group sums).
+// The 8 MMA steps of one K group of one tile, accumulated in one chain (the
+// group's partial sum, scaled once afterwards). OFFSET: the A operand holds
+// 136 + q (the caller corrects with the x group sums).
 template <bool OFFSET>
 __device__ __forceinline__ void stage_mma(const uint4& wA, const uint4& wB, const uint4 (&b)[4],
-                                          float (&t4)[4][4]) {
+                                          float (&t)[4]) {
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const uint32_t ra = word_of(wA, m), rb = word_of(wB, m);
@@ -272,7 +273,7 @@ __device__ __forceinline__ void stage_mma(const uint4& wA, const uint4& wB, cons
       a[2] = int4_pair_to_bf16x2<1>(ra);
       a[3] = int4_pair_to_bf16x2<1>(rb);
     }
-    mma_bf16_16816(t4[(2 * m) & 3], a, b[m].x, b[m].y, t4[(2 * m) & 3]);
+    mma_bf16_16816(t, a, b[m].x, b[m].y, t);
     if (OFFSET) {
       a[0] = int4_pair_to_bf16x2_offset<2>(ra);
       a[1] = int4_pair_to_bf16x2_offset<2>(rb);
@@ -284,7 +285,7 @@ __device__ __forceinline__ void stage_mma(const uint4& wA, const uint4& wB, cons
       a[2] = int4_pair_to_bf16x2<3>(ra);
       a[3] = int4_pair_to_bf16x2<3>(rb);
     }
-    mma_bf16_16816(t4[(2 * m + 1) & 3], a, b[m].z, b[m].w, t4[(2 * m + 1) & 3]);
+    mma_bf16_16816(t, a, b[m].z, b[m].w, t);
   }
 }
 
@@ -989,9 +990,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int m = 0; m < 4; ++m) b[m] = make_uint4(0u, 0u, 0u, 0u);
         }
-        // 2 tiles x 8 MMA steps in 8 independent chains (the x fragments are
+        // 2 tiles x 8 MMA steps, one chain per tile (the x fragments are
         // shared by both tiles)
-        float t4[2][4][4] = {};
+        float t4[2][4] = {};
         if (pre) {
           stage_mma<true>(wA[0], wB[0], b, t4[0]);
           stage_mma<true>(wA[1], wB[1], b, t4[1]);
@@ -1009,8 +1010,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tl = 0; tl < 2; ++tl) {
           float tmp[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            tmp[i] = (t4[tl][0][i] + t4[tl][1][i]) + (t4[tl][2][i] + t4[tl][3][i]);
+          for (int i = 0; i < 4; ++i) tmp[i] = t4[tl][i];
           if (pre) {
             tmp[0] = fmaf(-136.f, xs0, tmp[0]);
             tmp[1] = fmaf(-136.f, xs1, tmp[1]);
