@@ -784,8 +784,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm2r);
       prefetch_tmap(&tm2s);
     }
-    for (int tau = blockIdx.x; !stop; tau += gridDim.x) {
-      if (tau >= cnt.sh1 + cnt.sh2 && !known) {
+    // Tasks are decoded 32 at a time, lane l taking the CTA's l-th next task,
+    // and handed out one by one by shuffles: the per-task decode (a search
+    // over the active experts, divisions) runs once per 32 tasks. A batch
+    // never spans the shared/routed boundary, so shared work never waits for
+    // the routing.
+    const int sh_end = cnt.sh1 + cnt.sh2;
+    Task mine{};
+    int bi = 32;
+    for (int tau = blockIdx.x; !stop; tau += gridDim.x, ++bi) {
+      if (tau >= sh_end && !known) {
         // routed tasks: wait for this CTA's routing (shared memory)
         int ok = 1;
         if (lane == 0) ok = dwait(&s.route_ready, 0, err) ? 1 : 0;
@@ -795,8 +803,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         cnt.r1 = s.meta[1];
         cnt.r2 = s.meta[2];
         known = true;
+        bi = 32;  // the current batch (shared tasks) ends here
       }
-      const Task t = task_at(s, d, cnt, tau);
+      if (bi == 32) {
+        const int tl = tau + lane * (int)gridDim.x;
+        if ((tau < sh_end) == (tl < sh_end)) {
+          mine = task_at(s, d, cnt, tl);
+        } else {
+          mine = Task{};
+          mine.ngroups = 0;
+        }
+        bi = 0;
+      }
+      Task t;
+      t.down = __shfl_sync(0xffffffffu, mine.down ? 1 : 0, bi) != 0;
+      t.shared = __shfl_sync(0xffffffffu, mine.shared ? 1 : 0, bi) != 0;
+      t.e = __shfl_sync(0xffffffffu, mine.e, bi);
+      t.ngroups = __shfl_sync(0xffffffffu, mine.ngroups, bi);
+      t.rowA0 = __shfl_sync(0xffffffffu, mine.rowA0, bi);
+      t.rowA1 = __shfl_sync(0xffffffffu, mine.rowA1, bi);
+      t.r0 = __shfl_sync(0xffffffffu, mine.r0, bi);
+      t.nr = __shfl_sync(0xffffffffu, mine.nr, bi);
+      t.tile = __shfl_sync(0xffffffffu, mine.tile, bi);
+      t.pass = __shfl_sync(0xffffffffu, mine.pass, bi);
+      // past the last task (a batch that reached the end of the shared tasks
+      // was restarted above, where the routed range begins)
       if (t.ngroups == 0) break;
       if (lane == 0) {
         const CUtensorMap* tm = t.down ? (t.shared ? &tm2s : &tm2r) : (t.shared ? &tm13s : &tm13r);
