@@ -128,7 +128,11 @@ int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t num_tokens
 
 /* The same forward with HOST activations: copies x_host (bf16 [T, H]) to the
  * device, runs the forward, copies the result to out_host and synchronises
- * `stream`. Host buffers should be pinned for asynchronous copies. */
+ * `stream`. Host buffers should be pinned for asynchronous copies. With pinned
+ * buffers (and without FLAG_PROFILE) the copy-forward-copy sequence is
+ * recorded once into a CUDA graph owned by the handle and replayed while the
+ * buffers, num_tokens and the weight pointers stay the same; a change records
+ * it again. Calls must not overlap (the handle is single-stream). */
 int moe_w4a16_forward_host(moe_w4a16_handle* h, const uint16_t* x_host, int32_t num_tokens,
                            const moe_w4a16_weights* w, uint16_t* out_host, void* stream);
 

@@ -172,6 +172,20 @@ def test_tiny_forward_host_matches_device(tiny):
     oh = torch.empty((16, shape.hidden), dtype=torch.int16).pin_memory()
     obj.forward_host(xh, oh)
     np.testing.assert_array_equal(oh.numpy(), a)
+    # pinned buffers replay a recorded graph: new contents of the same buffer,
+    # then a different token count (a new recording), then pageable buffers
+    other = mc.layer_with_tokens(shape, 16, bias=None).x[::-1].copy()
+    b, _ = _run(obj, other)
+    xh.copy_(torch.from_numpy(other.view(np.int16)))
+    obj.forward_host(xh, oh)
+    np.testing.assert_array_equal(oh.numpy(), b)
+    oh5 = torch.empty((5, shape.hidden), dtype=torch.int16).pin_memory()
+    obj.forward_host(xh[:5], oh5)
+    np.testing.assert_array_equal(oh5.numpy(), b[:5])
+    ohp = torch.empty((16, shape.hidden), dtype=torch.int16)
+    obj.forward_host(torch.from_numpy(other.view(np.int16)), ohp)
+    np.testing.assert_array_equal(ohp.numpy(), b)
+    assert moe.moe_w4a16_check_device_errors(obj.handle) == 0
     obj.close()
 
 

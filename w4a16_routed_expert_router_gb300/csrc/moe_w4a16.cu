@@ -30,6 +30,14 @@ struct moe_w4a16_handle {
   uint16_t* x_dev = nullptr;    // forward_host staging
   uint16_t* out_dev = nullptr;
   int last_T = 0;
+  // forward_host with pinned buffers replays one CUDA graph (copy in, forward,
+  // copy out), recorded for these buffers, this token count and these weights
+  cudaStream_t capture_stream = nullptr;
+  cudaGraphExec_t host_graph = nullptr;
+  const void* hg_x = nullptr;
+  const void* hg_out = nullptr;
+  int hg_T = -1;
+  moe_w4a16_weights hg_w{};
   LaunchLog log;
   cudaEvent_t events[2 * LaunchLog::kMax];
   bool events_made = false;
@@ -72,6 +80,16 @@ EncodeTiledFn encode_fn() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Page-locked (or registered) host memory: copies from it can be captured.
+bool is_pinned(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -424,6 +442,8 @@ int moe_w4a16_destroy(moe_w4a16_handle* h) {
   cudaDeviceSynchronize();
   if (h->events_made)
     for (int i = 0; i < 2 * LaunchLog::kMax; ++i) cudaEventDestroy(h->events[i]);
+  if (h->host_graph) cudaGraphExecDestroy(h->host_graph);
+  if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
   if (h->ws) cudaFree(h->ws);
   delete h;
   return MOE_W4A16_OK;
@@ -586,6 +606,50 @@ int moe_w4a16_forward_host(moe_w4a16_handle* h, const uint16_t* x_host, int32_t 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t n = (size_t)T * h->cfg.hidden * 2;
   int st;
+  if (T > 0 && !(h->cfg.flags & MOE_W4A16_FLAG_PROFILE) && is_pinned(x_host) && is_pinned(out_host)) {
+    // one graph launch instead of three API calls per forward
+    cudaSetDevice(h->device);
+    if ((st = validate_weights(h->cfg, w)) != MOE_W4A16_OK) return st;
+    if (!h->host_graph || h->hg_x != x_host || h->hg_out != out_host || h->hg_T != T ||
+        memcmp(&h->hg_w, w, sizeof(*w)) != 0) {
+      if (h->host_graph) {
+        cudaGraphExecDestroy(h->host_graph);
+        h->host_graph = nullptr;
+      }
+      if (!h->capture_stream &&
+          (st = cuda_status(cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking))) !=
+              MOE_W4A16_OK)
+        return st;
+      cudaStream_t c = h->capture_stream;
+      if ((st = cuda_status(cudaStreamBeginCapture(c, cudaStreamCaptureModeThreadLocal))) !=
+          MOE_W4A16_OK)
+        return st;
+      cudaError_t e = cudaMemcpyAsync(h->x_dev, x_host, n, cudaMemcpyHostToDevice, c);
+      int fst = e == cudaSuccess ? moe_w4a16_forward(h, h->x_dev, T, w, h->out_dev, c) : MOE_W4A16_OK;
+      if (e == cudaSuccess && fst == MOE_W4A16_OK)
+        e = cudaMemcpyAsync(out_host, h->out_dev, n, cudaMemcpyDeviceToHost, c);
+      cudaGraph_t g = nullptr;
+      const cudaError_t ee = cudaStreamEndCapture(c, &g);
+      if (fst != MOE_W4A16_OK || e != cudaSuccess || ee != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        cudaGetLastError();
+        return fst != MOE_W4A16_OK ? fst : cuda_status(e != cudaSuccess ? e : ee);
+      }
+      e = cudaGraphInstantiate(&h->host_graph, g, 0);
+      cudaGraphDestroy(g);
+      if (e != cudaSuccess) {
+        h->host_graph = nullptr;
+        return cuda_status(e);
+      }
+      h->hg_x = x_host;
+      h->hg_out = out_host;
+      h->hg_T = T;
+      h->hg_w = *w;
+    }
+    if ((st = cuda_status(cudaGraphLaunch(h->host_graph, s))) != MOE_W4A16_OK) return st;
+    h->last_T = T;
+    return cuda_status(cudaStreamSynchronize(s));
+  }
   if (T > 0) {
     cudaSetDevice(h->device);
     if ((st = cuda_status(cudaMemcpyAsync(h->x_dev, x_host, n, cudaMemcpyHostToDevice, s))) !=
