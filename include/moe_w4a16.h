@@ -80,6 +80,7 @@ enum moe_w4a16_status {
 /* device error flag bits (moe_w4a16_check_device_errors) */
 #define MOE_W4A16_DEVERR_TIMEOUT 0x1u    /* a bounded wait gave up                */
 #define MOE_W4A16_DEVERR_RANGE 0x2u      /* an index left its range               */
+#define MOE_W4A16_DEVERR_LAYOUT 0x4u     /* shared memory not aligned as required */
 
 typedef struct moe_w4a16_config {
   int32_t hidden;        /* H: multiple of 128, <= 16384                         */

@@ -13,6 +13,7 @@ constexpr int kMaxTopK = 8;
 constexpr int kMaxExperts = 256;
 constexpr uint32_t kErrTimeout = 0x1u;
 constexpr uint32_t kErrRange = 0x2u;
+constexpr uint32_t kErrLayout = 0x4u;
 
 // Layer sizes as seen by every kernel.
 struct Dims {
@@ -171,17 +172,6 @@ __device__ __forceinline__ uint32_t int4_pair_to_bf16x2(uint32_t word) {
   const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
   b = __hsub2(b, off);
   return *reinterpret_cast<uint32_t*>(&b);
-}
-
-// The same two codes as bf16 128 + u (exact), without the subtraction: a
-// caller that subtracts 136 * sum(x) from the dot product afterwards gets the
-// same result up to fp32 rounding.
-template <int J>
-__device__ __forceinline__ uint32_t int4_pair_to_bf16x2_offset(uint32_t word) {
-  uint32_t v;
-  const uint32_t w = word >> (4 * J);
-  asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(v) : "r"(w), "r"(0x000F000Fu), "r"(0x43004300u));
-  return v;
 }
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {

@@ -10,7 +10,7 @@
 // a ramp-up and a tail of the memory pipeline, so the whole layer runs as one
 // task stream that never stops fetching weights:
 //
-//   [gate/up shared | down shared | gate/up routed | down routed]
+//   [gate/up shared | gate/up routed | down shared | down routed]
 //
 // CTA b takes tasks b, b + G, b + 2G, ... (G = one CTA per SM). A task covers
 // two 16-row weight tiles (16 gate + 16 up channels, or 32 down channels) of
@@ -25,24 +25,24 @@
 //    scan, stable permutation, task lists). Computing it redundantly per CTA
 //    keeps the critical path at two global round trips, and it overlaps the
 //    shared expert's work, which needs no routing.
-//  * 8 consumer warps stream stages from the start: warp w takes K-group w
-//    of both tiles (the activation fragments serve both; one MMA chain per
-//    tile); exact INT4 -> bf16 in registers, mma.sync m16n8k16
-//    with weights as A and up to 8 rows as B, group scales applied in fp32. At the end of a task each warp drops its partial sums into a
-//    slot and moves on. Routed gate/up stages skip two steps: their x rows
-//    come pre-interleaved, and the weights stay 136 + q (one op per code
-//    pair) with 136 * sum(x over the group) taken off each group's dot
-//    product; every CTA interleaves and sums its share of the tokens once per
-//    forward, before the logits are published.
-//  * 1 weight producer warp: decodes tasks and fills a ring of stages (2-D TMA
-//    boxes of 16 rows x 512 B per tile, scale boxes) with a descriptor per
+//  * 8 consumer warps stream stages from the start: warp w takes K-group w of
+//    both tiles (the activation fragments serve both; one MMA chain per
+//    tile); exact INT4 -> bf16 in registers (lop3 into the mantissa, a bf16x2
+//    subtract), mma.sync m16n8k16 with the weights as A and up to 8 rows as
+//    B, group scales applied in fp32. At the end of a task each warp drops its
+//    partial sums into a slot and moves on. Every stage reads its activation
+//    rows (the interleaved x that the CTAs owning a token prepare once per
+//    forward, or h) in one layout, so all stages share one code path.
+//  * 1 weight producer warp: decodes tasks and fills a ring of stages (TMA
+//    boxes of 16 rows x 512 B per tile, 128-byte swizzled when K is a
+//    multiple of 256, and scale boxes) with a descriptor per
 //    stage; it only ever waits for free stages, so the weight stream never
 //    stops on a dependency. A stage holds the weights plus room for the
 //    pass's activation rows (min(T, 8)), so a small batch gets more stages:
 //    at one token about 11 stages (176 KB of weights in flight per SM) instead
 //    of 5, enough to cover the ~1.5 us a weight box takes to arrive.
 //  * 1 activation warp: in ring order, copies each stage's activation rows
-//    (x for gate/up, h for down) into the stage (1-D bulk copies). Down tasks
+//    (interleaved x for gate/up, h for down) into the stage (1-D bulk copies). Down tasks
 //    need the h rows of their (expert, pass): it polls the completion counters
 //    of every active (expert, pass) at once (lanes in parallel, one round trip)
 //    and keeps the finished ones in a shared-memory bitmap.
@@ -85,8 +85,14 @@ constexpr int kMaxPass = (kSmallT + kR - 1) / kR;  // passes per expert at most
 constexpr int kPairs = (kMaxExperts + 1) * kMaxPass;  // (expert, pass) counters
 constexpr int kItems = kSmallT * kMaxTopK;
 
-enum { kFirst = 1, kLast = 2, kEnd = 4, kShared = 8, kDown = 16, kPre = 32 };
-constexpr int kXSumO = 8 * 256;              // group sums of a row, in its slot's padding
+// Stage descriptor flags. The consumers read only this word of a stage's
+// descriptor: the K groups of the stage sit in bits 8-11 and the activation
+// rows in bits 12-15.
+// kPre: a gate/up stage, whose activation rows are the interleaved x.
+enum { kFirst = 1, kLast = 2, kEnd = 4, kShared = 8, kDown = 16, kPre = 32, kSwz = 64 };
+__host__ __device__ constexpr int stage_key(int flags, int gcnt, int nr) {
+  return flags | (gcnt << 8) | (nr << 12);
+}
 
 struct Desc {
   int flags, g0, gcnt, ngroups, tile, r0, nr, rowA0, rowA1, cnt, pad[2];  // cnt: (expert, pass)
@@ -136,8 +142,6 @@ struct DecodeParams {
   const uint16_t* s2_routed;
   const uint16_t* s2_shared;
   uint16_t* xi;                 // [T, H] bf16: x interleaved, chunks transposed (chunk_t)
-  float* xs;                    // [T, xs_stride] fp32: sum of x over each K group
-  int xs_stride;                // H / 128 rounded up to 8 (32-byte rows)
   uint16_t* h;                  // [rows, hstride] bf16, interleaved, chunks transposed
   int hstride;
   float* y;                     // [rows, H] fp32
@@ -237,6 +241,24 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, uin
       : "memory");
 }
 
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
+                                       int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// A weight matrix whose rows are a whole number of 128-byte segments (K a
+// multiple of 256) is fetched as a 3-D box {32 words, 4 segments, 16 rows}
+// with the 128-byte swizzle: 16-byte chunk q of the 128-byte line at byte
+// offset o of the tile lands at chunk q ^ ((o >> 7) & 7). Rows 512 bytes apart
+// then differ in bit 2 of the swizzle, so the two rows read by a quarter warp
+// fall in opposite halves of the banks. Other matrices keep the plain 2-D box
+// (16 rows x 512 bytes, row-major).
+__device__ __forceinline__ bool swizzled_k(int K) { return K % 256 == 0; }
+
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
   return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
 }
@@ -246,45 +268,24 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
 // K group (w = 4c + m: lane column c, MMA step m) at position 4m + c.
 __device__ __forceinline__ int chunk_t(int w) { return ((w & 3) << 2) | (w >> 2); }
 
-__device__ __forceinline__ float lds_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-  return v;
-}
-
 // The 8 MMA steps of one K group of one tile, accumulated in one chain (the
-// group's partial sum, scaled once afterwards). OFFSET: the A operand holds
-// 136 + q (the caller corrects with the x group sums).
-template <bool OFFSET>
+// group's partial sum, scaled once afterwards): each code pair becomes bf16
+// q exactly (lop3 into the mantissa, then a bf16x2 subtract).
 __device__ __forceinline__ void stage_mma(const uint4& wA, const uint4& wB, const uint4 (&b)[4],
                                           float (&t)[4]) {
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const uint32_t ra = word_of(wA, m), rb = word_of(wB, m);
     uint32_t a[4];
-    if (OFFSET) {
-      a[0] = int4_pair_to_bf16x2_offset<0>(ra);
-      a[1] = int4_pair_to_bf16x2_offset<0>(rb);
-      a[2] = int4_pair_to_bf16x2_offset<1>(ra);
-      a[3] = int4_pair_to_bf16x2_offset<1>(rb);
-    } else {
-      a[0] = int4_pair_to_bf16x2<0>(ra);
-      a[1] = int4_pair_to_bf16x2<0>(rb);
-      a[2] = int4_pair_to_bf16x2<1>(ra);
-      a[3] = int4_pair_to_bf16x2<1>(rb);
-    }
+    a[0] = int4_pair_to_bf16x2<0>(ra);
+    a[1] = int4_pair_to_bf16x2<0>(rb);
+    a[2] = int4_pair_to_bf16x2<1>(ra);
+    a[3] = int4_pair_to_bf16x2<1>(rb);
     mma_bf16_16816(t, a, b[m].x, b[m].y, t);
-    if (OFFSET) {
-      a[0] = int4_pair_to_bf16x2_offset<2>(ra);
-      a[1] = int4_pair_to_bf16x2_offset<2>(rb);
-      a[2] = int4_pair_to_bf16x2_offset<3>(ra);
-      a[3] = int4_pair_to_bf16x2_offset<3>(rb);
-    } else {
-      a[0] = int4_pair_to_bf16x2<2>(ra);
-      a[1] = int4_pair_to_bf16x2<2>(rb);
-      a[2] = int4_pair_to_bf16x2<3>(ra);
-      a[3] = int4_pair_to_bf16x2<3>(rb);
-    }
+    a[0] = int4_pair_to_bf16x2<2>(ra);
+    a[1] = int4_pair_to_bf16x2<2>(rb);
+    a[2] = int4_pair_to_bf16x2<3>(ra);
+    a[3] = int4_pair_to_bf16x2<3>(rb);
     mma_bf16_16816(t, a, b[m].z, b[m].w, t);
   }
 }
@@ -332,20 +333,23 @@ __device__ __forceinline__ int find_active(const int* pre, int n_act, int tau) {
   return lo;
 }
 
-// Task tau of the concatenated list [gate/up shared | down shared | gate/up
-// routed | down routed], or t.ngroups == 0 when tau is past its end.
+// Task tau of the concatenated list [gate/up shared | gate/up routed | down
+// shared | down routed], or t.ngroups == 0 when tau is past its end. Only the
+// first part needs no routing; every CTA takes all its gate/up tasks before
+// its down tasks, and the shared down work sits between the two routed halves
+// so that the routed gate/up stream starts as soon as the routing is known.
 __device__ __forceinline__ Task task_at(const Smem& s, const Dims& d, const Counts& c, int tau) {
   const int sh0 = d.T * d.k, sh1 = d.T * d.k + d.T;
   if (tau < c.sh1) return make_task(d, false, true, d.E, sh0, sh1, tau);
   tau -= c.sh1;
-  if (tau < c.sh2) return make_task(d, true, true, d.E, sh0, sh1, tau);
-  tau -= c.sh2;
   if (tau < c.r1) {
     const int a = find_active(s.pre1, c.n_act, tau);
     const int e = s.active[a];
     return make_task(d, false, false, e, s.offsets[e], s.offsets[e + 1], tau - s.pre1[a]);
   }
   tau -= c.r1;
+  if (tau < c.sh2) return make_task(d, true, true, d.E, sh0, sh1, tau);
+  tau -= c.sh2;
   if (tau < c.r2) {
     const int a = find_active(s.pre2, c.n_act, tau);
     const int e = s.active[a];
@@ -578,35 +582,20 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
   for (int e = tid; e < d.E; e += kRW * 32) s.bias_s[e] = __ldg(p.router_bias + e);
   score_experts(s, p, warp);
   // publish this CTA's logits, then (off the logits' critical path) the
-  // interleaved x and group sums, then wait for everybody's logits
+  // interleaved x, then wait for everybody's logits
   if (tid == 0) {
     __threadfence();
     atomicAdd(&p.sync[0], 1u);
   }
-  // this CTA's share of the tokens (t = b, b + G, ...): interleaved copy and
-  // per-group sums of x for the routed gate/up stages of every CTA; published on
-  // their own counter
+  // this CTA's share of the tokens (t = b, b + G, ...): the interleaved copy
+  // of x that every CTA's gate/up stages read; published on its own counter
   {
     const int h8 = d.H / 8;  // 16-byte chunks of a row; 16 per K group
     for (int t = blockIdx.x; t < d.T; t += gridDim.x) {
       const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * d.H);
       uint4* dst = reinterpret_cast<uint4*>(p.xi + (size_t)t * d.H);
-      for (int c0 = 0; c0 < h8; c0 += kRW * 32) {
-        const int cidx = c0 + tid;
-        float part = 0.f;
-        if (cidx < h8) {
-          const uint4 v = __ldg(src + cidx);
-          dst[(cidx & ~15) | chunk_t(cidx & 15)] = interleave8(v);
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            part += __uint_as_float(w4[q] << 16) + __uint_as_float(w4[q] & 0xffff0000u);
-        }
-        // the 16 chunks of a group sit in 16 consecutive lanes
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if (cidx < h8 && (cidx & 15) == 0) p.xs[(size_t)t * p.xs_stride + (cidx >> 4)] = part;
-      }
+      for (int cidx = tid; cidx < h8; cidx += kRW * 32)
+        dst[(cidx & ~15) | chunk_t(cidx & 15)] = interleave8(__ldg(src + cidx));
     }
   }
   rbar();
@@ -751,6 +740,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Dims& d = p.d;
   unsigned* err = p.r.err;
   const bool scale_tma = p.scale_tma != 0;
+  // swizzled weight boxes need 1024-byte aligned stages; every thread of every
+  // CTA sees the same address, so all of them leave before any barrier
+  if (smem_u32(stage_base) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(err, kErrLayout);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.nst; ++i) {
@@ -787,9 +782,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Tasks are decoded 32 at a time, lane l taking the CTA's l-th next task,
     // and handed out one by one by shuffles: the per-task decode (a search
     // over the active experts, divisions) runs once per 32 tasks. A batch
-    // never spans the shared/routed boundary, so shared work never waits for
-    // the routing.
-    const int sh_end = cnt.sh1 + cnt.sh2;
+    // never spans the end of the routing-free part (the shared gate/up
+    // tasks), so that work never waits for the routing.
+    const int sh_end = cnt.sh1;
     Task mine{};
     int bi = 32;
     for (int tau = blockIdx.x; !stop; tau += gridDim.x, ++bi) {
@@ -832,6 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const CUtensorMap* tm = t.down ? (t.shared ? &tm2s : &tm2r) : (t.shared ? &tm13s : &tm13r);
         const CUtensorMap* ts = t.down ? (t.shared ? &ts2s : &ts2r) : (t.shared ? &ts13s : &ts13r);
+        const bool swz = swizzled_k(t.ngroups * kGroup);
         for (int g0 = 0; g0 < t.ngroups; g0 += 8) {
           const int gcnt = min(8, t.ngroups - g0);
           if (!dwait(&s.empty[stage], phase ^ 1u, err)) {
@@ -839,9 +835,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           Desc& ds = s.desc[stage];
-          const bool pre = !t.shared && !t.down;
-          ds.flags = (g0 == 0 ? kFirst : 0) | (g0 + 8 >= t.ngroups ? kLast : 0) |
-                     (t.shared ? kShared : 0) | (t.down ? kDown : 0) | (pre ? kPre : 0);
+          const bool pre = !t.down;  // gate/up: the interleaved x rows
+          ds.flags = stage_key((g0 == 0 ? kFirst : 0) | (g0 + 8 >= t.ngroups ? kLast : 0) |
+                                   (t.shared ? kShared : 0) | (t.down ? kDown : 0) |
+                                   (pre ? kPre : 0) | (swz ? kSwz : 0),
+                               gcnt, t.nr);
           ds.g0 = g0;
           ds.gcnt = gcnt;
           ds.ngroups = t.ngroups;
@@ -853,11 +851,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           ds.cnt = t.e * kMaxPass + t.pass;
           // the activation warp copies nr rows into the stage; a TMA box always
           // delivers its full size (out-of-range parts are zero-filled)
-          mbar_arrive_expect_tx(&s.full[stage],
-                                kWB + (scale_tma ? kSB : 0) + t.nr * (gcnt * 256 + (pre ? 32 : 0)));
+          mbar_arrive_expect_tx(&s.full[stage], kWB + (scale_tma ? kSB : 0) + t.nr * gcnt * 256);
           uint8_t* st = stage_base + (size_t)stage * sb;
-          tma_2d(smem_u32(st), tm, &s.full[stage], g0 * 16, t.rowA0);
-          tma_2d(smem_u32(st + kWB / 2), tm, &s.full[stage], g0 * 16, t.rowA1);
+          if (swz) {
+            tma_3d(smem_u32(st), tm, &s.full[stage], 0, g0 / 2, t.rowA0);
+            tma_3d(smem_u32(st + kWB / 2), tm, &s.full[stage], 0, g0 / 2, t.rowA1);
+          } else {
+            tma_2d(smem_u32(st), tm, &s.full[stage], g0 * 16, t.rowA0);
+            tma_2d(smem_u32(st + kWB / 2), tm, &s.full[stage], g0 * 16, t.rowA1);
+          }
           if (scale_tma) {
             tma_2d(smem_u32(st + kWB), ts, &s.full[stage], g0, t.rowA0);
             tma_2d(smem_u32(st + kWB + kSB / 2), ts, &s.full[stage], g0, t.rowA1);
@@ -935,8 +937,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async();
       }
       if ((ds.flags & kPre) && !pre_ready) {
-        // interleaved x and group sums come from other CTAs' generic stores,
-        // published on their own counter by the CTAs that own a token
+        // the interleaved x comes from other CTAs' generic stores, published
+        // on its own counter by the CTAs that own a token
         int ok = 1;
         if (lane == 0)
           ok = wait_counter(reinterpret_cast<const int*>(p.sync + 1), min(d.T, (int)gridDim.x), err) ? 1 : 0;
@@ -949,12 +951,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = ds.r0 + lane;
         const uint32_t slot = smem_u32(stage_base + (size_t)stage * sb + kXO + lane * kXS);
         const uint16_t* src;
-        if (ds.flags & kPre) {
-          const int tok = s.perm_s[r];
+        if (!down) {
+          const int tok = (ds.flags & kShared) ? r - d.T * d.k : s.perm_s[r];
           src = p.xi + (size_t)tok * d.H;
-          bulk_copy(slot + kXSumO, p.xs + (size_t)tok * p.xs_stride + ds.g0, 32, &s.full[stage]);
-        } else if (!down) {
-          src = p.x + (size_t)((ds.flags & kShared) ? r - d.T * d.k : r) * d.H;
         } else {
           src = p.h + (size_t)r * p.hstride;
         }
@@ -971,8 +970,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int gw = warp;  // K group of the stage; both 16-row tiles
     const uint32_t stage0 = smem_u32(stage_base);
     const uint32_t w_off = g * 512 + gw * 64 + c * 16;
+    // the same 16 bytes in a swizzled tile (rows g and g + 8 share the pattern)
+    const uint32_t seg = (uint32_t)gw >> 1;
+    const uint32_t w_off_s =
+        g * 512 + seg * 128 + (((((uint32_t)(gw & 1) << 2) | c) ^ (seg | ((uint32_t)(g & 1) << 2))) << 4);
     const uint32_t s_off = kWB + g * 16 + gw * 2;
-    const uint32_t x_off = kXO + g * kXS + gw * 256 + c * 64;  // natural chunk order
     const uint32_t xt_off = kXO + g * kXS + gw * 256 + c * 16;  // transposed (xi, h)
     int stage = 0;
     uint32_t phase = 0;
@@ -980,43 +982,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     float acc[2][4] = {};
     for (;;) {
       if (!dwait(&s.full[stage], phase, err)) break;
-      const Desc ds = s.desc[stage];
-      if (ds.flags & kEnd) break;
-      if (ds.flags & kFirst) {
+      const int key = s.desc[stage].flags;  // one shared-memory word per stage
+      if (key & kEnd) break;
+      if (key & kFirst) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[0][i] = acc[1][i] = 0.f;
       }
-      if (gw < ds.gcnt) {
+      const int gcnt = (key >> 8) & 15, nr = (key >> 12) & 15;
+      if (gw < gcnt) {
         const uint32_t st = stage0 + stage * sb;
+        const uint32_t wo = (key & kSwz) ? w_off_s : w_off;
         uint4 wA[2], wB[2];
         float sc[2][2];  // [tile][row g / g + 8]
 #pragma unroll
         for (int tl = 0; tl < 2; ++tl) {
-          wA[tl] = lds128(st + tl * (kWB / 2) + w_off);
-          wB[tl] = lds128(st + tl * (kWB / 2) + w_off + 8 * 512);
+          wA[tl] = lds128(st + tl * (kWB / 2) + wo);
+          wB[tl] = lds128(st + tl * (kWB / 2) + wo + 8 * 512);
           if (scale_tma) {
             sc[tl][0] = bf16_bits_to_f32(lds16(st + tl * (kSB / 2) + s_off));
             sc[tl][1] = bf16_bits_to_f32(lds16(st + tl * (kSB / 2) + s_off + 8 * 16));
           } else {
-            const uint16_t* scl = (ds.flags & kDown) ? ((ds.flags & kShared) ? p.s2_shared : p.s2_routed)
-                                                     : ((ds.flags & kShared) ? p.s13_shared : p.s13_routed);
-            const int row = (tl ? ds.rowA1 : ds.rowA0) + g;
-            sc[tl][0] = bf16_bits_to_f32(__ldg(scl + (size_t)row * ds.ngroups + ds.g0 + gw));
-            sc[tl][1] = bf16_bits_to_f32(__ldg(scl + (size_t)(row + 8) * ds.ngroups + ds.g0 + gw));
+            const Desc& dd = s.desc[stage];
+            const uint16_t* scl = (key & kDown) ? ((key & kShared) ? p.s2_shared : p.s2_routed)
+                                                : ((key & kShared) ? p.s13_shared : p.s13_routed);
+            const int row = (tl ? dd.rowA1 : dd.rowA0) + g;
+            sc[tl][0] = bf16_bits_to_f32(__ldg(scl + (size_t)row * dd.ngroups + dd.g0 + gw));
+            sc[tl][1] = bf16_bits_to_f32(__ldg(scl + (size_t)(row + 8) * dd.ngroups + dd.g0 + gw));
           }
         }
-        const bool pre = (ds.flags & kPre) != 0;
+        // activation rows (interleaved x, or h) store chunk 4c + m of a K
+        // group at 4m + c: the 4 lanes of a row read 64 contiguous bytes per
+        // step (no bank conflicts)
         uint4 b[4];
-        if (g < ds.nr) {
-          if (ds.flags & (kDown | kPre)) {
-            // chunk 4c + m of the group sits at 4m + c: the 4 lanes of a row
-            // read 64 contiguous bytes per step (no bank conflicts)
+        if (g < nr) {
 #pragma unroll
-            for (int m = 0; m < 4; ++m) b[m] = lds128(st + xt_off + m * 64);
-          } else {
-#pragma unroll
-            for (int m = 0; m < 4; ++m) b[m] = interleave8(lds128(st + x_off + m * 16));
-          }
+          for (int m = 0; m < 4; ++m) b[m] = lds128(st + xt_off + m * 64);
         } else {
 #pragma unroll
           for (int m = 0; m < 4; ++m) b[m] = make_uint4(0u, 0u, 0u, 0u);
@@ -1024,53 +1024,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 2 tiles x 8 MMA steps, one chain per tile (the x fragments are
         // shared by both tiles)
         float t4[2][4] = {};
-        if (pre) {
-          stage_mma<true>(wA[0], wB[0], b, t4[0]);
-          stage_mma<true>(wA[1], wB[1], b, t4[1]);
-        } else {
-          stage_mma<false>(wA[0], wB[0], b, t4[0]);
-          stage_mma<false>(wA[1], wB[1], b, t4[1]);
-        }
-        float xs0 = 0.f, xs1 = 0.f;
-        if (pre) {
-          // the weights were 136 + q: take 136 * sum(x) of tokens 2c, 2c + 1 off
-          if (2 * c < ds.nr) xs0 = lds_f32(st + kXO + 2 * c * kXS + kXSumO + gw * 4);
-          if (2 * c + 1 < ds.nr) xs1 = lds_f32(st + kXO + (2 * c + 1) * kXS + kXSumO + gw * 4);
-        }
+        stage_mma(wA[0], wB[0], b, t4[0]);
+        stage_mma(wA[1], wB[1], b, t4[1]);
 #pragma unroll
         for (int tl = 0; tl < 2; ++tl) {
-          float tmp[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) tmp[i] = t4[tl][i];
-          if (pre) {
-            tmp[0] = fmaf(-136.f, xs0, tmp[0]);
-            tmp[1] = fmaf(-136.f, xs1, tmp[1]);
-            tmp[2] = fmaf(-136.f, xs0, tmp[2]);
-            tmp[3] = fmaf(-136.f, xs1, tmp[3]);
-          }
-          acc[tl][0] = fmaf(sc[tl][0], tmp[0], acc[tl][0]);
-          acc[tl][1] = fmaf(sc[tl][0], tmp[1], acc[tl][1]);
-          acc[tl][2] = fmaf(sc[tl][1], tmp[2], acc[tl][2]);
-          acc[tl][3] = fmaf(sc[tl][1], tmp[3], acc[tl][3]);
+          acc[tl][0] = fmaf(sc[tl][0], t4[tl][0], acc[tl][0]);
+          acc[tl][1] = fmaf(sc[tl][0], t4[tl][1], acc[tl][1]);
+          acc[tl][2] = fmaf(sc[tl][1], t4[tl][2], acc[tl][2]);
+          acc[tl][3] = fmaf(sc[tl][1], t4[tl][3], acc[tl][3]);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.empty[stage]);
+      if (key & kLast) {
+        // end of a task: hand the partial sums to the slot's epilogue warp;
+        // the stage's descriptor is copied before the stage is released
+        const int b = tseq % kEW;
+        const uint32_t use = (uint32_t)(tseq / kEW);
+        if (!dwait(&s.slot_free[b], (use & 1u) ^ 1u, err)) break;
+        if (warp == 0 && lane == 0) s.slot_desc[b] = s.desc[stage];
+        s.red[b][warp * 32 + lane] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+        s.red[b][(8 + warp) * 32 + lane] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&s.empty[stage]);
+          mbar_arrive(&s.slot_full[b]);
+        }
+        ++tseq;
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.empty[stage]);
+      }
       if (++stage == nst) {
         stage = 0;
         phase ^= 1u;
       }
-      if (!(ds.flags & kLast)) continue;
-      // end of a task: hand the partial sums to the slot's epilogue warp
-      const int b = tseq % kEW;
-      const uint32_t use = (uint32_t)(tseq / kEW);
-      if (!dwait(&s.slot_free[b], (use & 1u) ^ 1u, err)) break;
-      s.red[b][warp * 32 + lane] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
-      s.red[b][(8 + warp) * 32 + lane] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
-      if (warp == 0 && lane == 0) s.slot_desc[b] = ds;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.slot_full[b]);
-      ++tseq;
     }
     // end of work: one end marker per epilogue warp
     for (int j = 0; j < kEW; ++j) {
@@ -1211,12 +1197,10 @@ cudaError_t decode_setup(int* ctas_per_sm) {
                                                        kStageOff + nst * sb);
 }
 
-int decode_xs_stride(int H) { return (H / kGroup + 7) / 8 * 8; }
-
 size_t decode_counter_ints(int E, int H) { return (size_t)(E + 1) * kMaxPass + H / kTile2 + 4; }
 
 cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& w, const uint16_t* x,
-                          uint16_t* xi, float* xs, uint16_t* h, int hstride, float* y, uint16_t* out,
+                          uint16_t* xi, uint16_t* h, int hstride, float* y, uint16_t* out,
                           int* counters, int grid, cudaStream_t s, LaunchLog& log) {
   DecodeParams p{};
   p.d = d;
@@ -1229,8 +1213,6 @@ cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& 
   p.s2_routed = w.s2_routed;
   p.s2_shared = w.s2_shared;
   p.xi = xi;
-  p.xs = xs;
-  p.xs_stride = decode_xs_stride(d.H);
   p.h = h;
   p.hstride = hstride;
   p.y = y;

@@ -74,7 +74,9 @@ struct DecodeWeights {
   const uint16_t* s13_shared;
   const uint16_t* s2_routed;
   const uint16_t* s2_shared;
-  // 2-D views of the packed weights {K/8 words, rows}, box {128 words, 16 rows}
+  // views of the packed weights, 8 K-groups of 16 rows per box: 3-D
+  // {32 words, K/256, rows} with the 128-byte swizzle when K % 256 == 0, else
+  // 2-D {K/8 words, rows}
   CUtensorMap tm13r, tm13s, tm2r, tm2s;
   // 2-D views of the scales {K/128, rows}, box {8, 16} (when scale_tma)
   CUtensorMap ts13r, ts13s, ts2r, ts2s;
@@ -82,11 +84,10 @@ struct DecodeWeights {
 };
 cudaError_t decode_setup(int* ctas_per_sm);
 size_t decode_counter_ints(int E, int H);
-// xi: [T, H] bf16 scratch (x interleaved), xs: [T, decode_xs_stride(H)] fp32
-// scratch (x summed over each K group), both written by the kernel itself.
-int decode_xs_stride(int H);
+// xi: [T, H] bf16 scratch, x interleaved with its 16-byte chunks transposed
+// within each K group, written by the kernel itself.
 cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& w, const uint16_t* x,
-                          uint16_t* xi, float* xs, uint16_t* h, int hstride, float* y, uint16_t* out,
+                          uint16_t* xi, uint16_t* h, int hstride, float* y, uint16_t* out,
                           int* counters, int grid, cudaStream_t s, LaunchLog& log);
 
 // Tensor-core (tcgen05) expert GEMMs for large batches.

@@ -53,7 +53,6 @@ struct moe_w4a16_handle {
   CUtensorMap xmap, hmap;
   // tensor-core router: bf16 planes of router_w and the view of this call's x
   uint16_t* planes = nullptr;
-  float* xs = nullptr;          // decode: x summed per K group (x interleaved lives in xperm)
   CUtensorMap wmap_router, xmap_router;
   const void* xmap_key = nullptr;
   int xmap_rows = 0;
@@ -152,7 +151,6 @@ Layout plan(const moe_w4a16_config& c) {
       (E + 2) * 4,           // 22 task3
       (E + 2) * 4,           // 23 task4
       3 * E * H * 2,         // 24 router planes
-      Tm * decode_xs_stride(c.hidden) * 4,  // 25 decode: x summed per K group
   };
   Layout L;
   size_t o = 0;
@@ -209,20 +207,35 @@ int encode_scale_map(CUtensorMap* m, const void* base, long long rows, int K) {
   return MOE_W4A16_OK;
 }
 
-// 2-D view {K/8 words, rows} of a packed INT4 tensor [rows, K/8] uint32, box
-// {128 words, 16 rows}: 8 K-groups of 16 rows (8 KB).
-int encode_int4_map2d(CUtensorMap* m, const void* base, long long rows, int K) {
+// Decode-kernel view of a packed INT4 tensor [rows, K/8] uint32: 8 K-groups
+// of 16 rows (8 KB) per box. When K is a multiple of 256 the rows are viewed
+// as 128-byte segments, {32 words, K/256 segments, rows}, box {32, 4, 16},
+// with the 128-byte swizzle (the consumers then read without bank
+// conflicts); otherwise a plain 2-D view {K/8 words, rows}, box {128, 16}.
+// The kernel picks its box form by the same rule.
+int encode_int4_map_decode(CUtensorMap* m, const void* base, long long rows, int K) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return MOE_W4A16_ERR_CUDA;
-  cuuint64_t dims[2] = {(cuuint64_t)K / 8, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K / 2};
-  cuuint32_t box[2] = {128, 16};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if (K % 256 == 0) {
+    cuuint64_t dims[3] = {32, (cuuint64_t)(K / 256), (cuuint64_t)rows};
+    cuuint64_t strides[2] = {128, (cuuint64_t)K / 2};
+    cuuint32_t box[3] = {32, 4, 16};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[2] = {(cuuint64_t)K / 8, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K / 2};
+    cuuint32_t box[2] = {128, 16};
+    cuuint32_t estr[2] = {1, 1};
+    r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) {
-    fprintf(stderr, "moe_w4a16: cuTensorMapEncodeTiled (2-D) failed (%d)\n", (int)r);
+    fprintf(stderr, "moe_w4a16: cuTensorMapEncodeTiled (decode weights) failed (%d)\n", (int)r);
     return MOE_W4A16_ERR_CUDA;
   }
   return MOE_W4A16_OK;
@@ -265,7 +278,7 @@ int get_map(moe_w4a16_handle* h, int slot, const void* base, long long rows, int
   if (h->map_keys[slot] == base && base) return MOE_W4A16_OK;
   const int st = slot < 4    ? encode_int4_map(&h->maps[slot], base, rows, K)
                  : slot < 8  ? encode_scale_map(&h->maps[slot], base, rows, K)
-                 : slot < 12 ? encode_int4_map2d(&h->maps[slot], base, rows, K)
+                 : slot < 12 ? encode_int4_map_decode(&h->maps[slot], base, rows, K)
                              : encode_int4_map_tc(&h->maps[slot], base, rows, K);
   if (st == MOE_W4A16_OK) h->map_keys[slot] = base;
   return st;
@@ -412,7 +425,6 @@ int moe_w4a16_create(const moe_w4a16_config* cfg, int device, moe_w4a16_handle**
   r.task3 = reinterpret_cast<int*>(b + L.off[22]);
   r.task4 = reinterpret_cast<int*>(b + L.off[23]);
   h->planes = reinterpret_cast<uint16_t*>(b + L.off[24]);
-  h->xs = reinterpret_cast<float*>(b + L.off[25]);
   if (h->tc_ok) {
     const long long rows = (long long)cfg->max_tokens * (cfg->top_k + 1);
     if ((st = encode_act_map_tc(&h->xmap, r.xperm, cfg->hidden, rows)) != MOE_W4A16_OK ||
@@ -537,7 +549,7 @@ int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t T, const m
     dw.ts2r = g2.ts_routed;
     dw.ts2s = g2.ts_shared;
     dw.scale_tma = scale_tma;
-    if ((e = launch_decode(d, h->r, dw, x, h->r.xperm, h->xs, h->h, h->hstride, h->y, out,
+    if ((e = launch_decode(d, h->r, dw, x, h->r.xperm, h->h, h->hstride, h->y, out,
                            h->counters, h->decode_grid, s, h->log)) != cudaSuccess)
       return cuda_status(e);
     h->last_T = T;
@@ -770,7 +782,6 @@ NoAllocLayout noalloc_plan(const moe_w4a16_config& c, int T) {
       rows * hstride * 2,                                // 13 h
       rows * H * 4,                                      // 14 y
       Tz * H * 2,                                        // 15 x interleaved
-      Tz * decode_xs_stride(c.hidden) * 4,               // 16 x group sums
   };
   NoAllocLayout L;
   size_t o = 0;
@@ -855,7 +866,6 @@ extern "C" int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint
   uint16_t* hbuf = reinterpret_cast<uint16_t*>(b + L.off[13]);
   float* ybuf = reinterpret_cast<float*>(b + L.off[14]);
   uint16_t* xibuf = reinterpret_cast<uint16_t*>(b + L.off[15]);
-  float* xsbuf = reinterpret_cast<float*>(b + L.off[16]);
   const int hstride = c.inter > c.shared_inter ? c.inter : c.shared_inter;
 
   // tensor maps, encoded on the host for this call
@@ -871,14 +881,14 @@ extern "C" int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint
   dw.s2_routed = w->w2_s;
   dw.s2_shared = has_sh ? w->sh_w2_s : w->w2_s;
   dw.scale_tma = scale_tma;
-  if ((st = encode_int4_map2d(&dw.tm13r, w->w13_q, r13, c.hidden)) != MOE_W4A16_OK) return st;
-  if ((st = encode_int4_map2d(&dw.tm2r, w->w2_q, r2, c.inter)) != MOE_W4A16_OK) return st;
+  if ((st = encode_int4_map_decode(&dw.tm13r, w->w13_q, r13, c.hidden)) != MOE_W4A16_OK) return st;
+  if ((st = encode_int4_map_decode(&dw.tm2r, w->w2_q, r2, c.inter)) != MOE_W4A16_OK) return st;
   dw.tm13s = dw.tm13r;
   dw.tm2s = dw.tm2r;
   if (has_sh) {
-    if ((st = encode_int4_map2d(&dw.tm13s, w->sh_w13_q, 2LL * c.shared_inter, c.hidden)) != MOE_W4A16_OK)
+    if ((st = encode_int4_map_decode(&dw.tm13s, w->sh_w13_q, 2LL * c.shared_inter, c.hidden)) != MOE_W4A16_OK)
       return st;
-    if ((st = encode_int4_map2d(&dw.tm2s, w->sh_w2_q, c.hidden, c.shared_inter)) != MOE_W4A16_OK)
+    if ((st = encode_int4_map_decode(&dw.tm2s, w->sh_w2_q, c.hidden, c.shared_inter)) != MOE_W4A16_OK)
       return st;
   }
   dw.ts13r = dw.tm13r;
@@ -907,5 +917,5 @@ extern "C" int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint
   Dims d{T, c.hidden, c.num_experts, c.top_k, c.inter, c.shared_inter};
   LaunchLog log;
   return cuda_status(
-      launch_decode(d, r, dw, x, xibuf, xsbuf, hbuf, hstride, ybuf, out, counters, nd.grid, s, log));
+      launch_decode(d, r, dw, x, xibuf, hbuf, hstride, ybuf, out, counters, nd.grid, s, log));
 }
