@@ -61,6 +61,29 @@ def test_tiny_layer_parity(tiny, T):
     obj.close()
 
 
+# hidden 384 (3 K-groups: a partial stage, the plain 2-D weight box), routed
+# intermediate 128 (plain box) against a shared intermediate of 256 (swizzled
+# box), group scales read without TMA; above 64 tokens the GEMV engine (the
+# tensor-core path needs hidden % 256 == 0)
+@pytest.fixture(scope="module")
+def odd():
+    shape = ms.MoeShape("odd384", 16, 384, 8, 2, 128, 256, 1006, 1006)
+    tensors = upload_layer(mc.weights_of(shape), DEV)[0]
+    return shape, tensors
+
+
+@pytest.mark.parametrize("T", [1, 5, 16, 64, 65, 130])
+def test_odd_shape_parity(odd, T):
+    shape, tensors = odd
+    layer = mc.layer_with_tokens(shape, T)
+    ref = mc.oracle(layer)
+    obj = _layer_obj(layer, tensors, max_tokens=256)
+    out, rt = _run(obj, layer.x)
+    mc.check_routing(rt, ref, shape.experts)
+    mc.check_output(out, ref["out"])
+    obj.close()
+
+
 @pytest.mark.parametrize("flags,T", [
     (moe.MOE_W4A16_FLAG_FORCE_TC, 1), (moe.MOE_W4A16_FLAG_FORCE_TC, 16),
     (moe.MOE_W4A16_FLAG_FORCE_TC, 64), (moe.MOE_W4A16_FLAG_FORCE_TC, 300),
