@@ -28,18 +28,29 @@ namespace {
 // to kPassRows rows of an expert's segment.
 __device__ __forceinline__ int passes_for(int rows) { return (rows + kPassRows - 1) / kPassRows; }
 
-// Warp-wide top-k of one token. Lane l holds experts l, l+32, ...; returns in
-// lanes 0..k-1 the chosen expert (descending sel, ties -> lower index) and its
-// unbiased score.
-__device__ __forceinline__ void warp_topk(const float* logit_row, const float* bias, int E, int k,
-                                          int lane, int* out_id, float* out_w) {
-  constexpr int kPer = kMaxExperts / 32;
+constexpr int kPer = kMaxExperts / 32;  // logits per lane
+
+// The logits of one token into registers: lane l takes experts l, l+32, ...
+__device__ __forceinline__ void load_row(const float* logit_row, int E, int lane,
+                                         float (&lg)[kPer]) {
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    lg[i] = e < E ? __ldcg(logit_row + e) : 0.f;
+  }
+}
+
+// Warp-wide top-k of one token whose logits lane l holds for experts l, l+32,
+// ...; returns in lanes 0..k-1 the chosen expert (descending sel, ties ->
+// lower index) and its unbiased score.
+__device__ __forceinline__ void warp_topk_regs(const float (&lg)[kPer], const float* bias, int E,
+                                               int k, int lane, int* out_id, float* out_w) {
   float sel[kPer], sc[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int e = lane + 32 * i;
     if (e < E) {
-      const float l = logit_row[e];
+      const float l = lg[i];
       const float s = 1.0f / (1.0f + expf(-l));
       sc[i] = s;
       sel[i] = s + bias[e];
@@ -89,6 +100,18 @@ __device__ __forceinline__ void warp_topk(const float* logit_row, const float* b
   for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, chosen_s, j);
   *out_id = chosen_e;
   *out_w = chosen_s / sum;
+}
+
+// The same, reading the token's logits from a row in memory.
+__device__ __forceinline__ void warp_topk(const float* logit_row, const float* bias, int E, int k,
+                                          int lane, int* out_id, float* out_w) {
+  float lg[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    lg[i] = e < E ? logit_row[e] : 0.f;
+  }
+  warp_topk_regs(lg, bias, E, k, lane, out_id, out_w);
 }
 
 // Exclusive scan of four values per thread across a 256-thread block;
@@ -354,16 +377,28 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
   __shared__ int hist[kMaxExperts];
   __shared__ int counts_s[kMaxExperts];
   __shared__ int offs_s[kMaxExperts];
+  __shared__ float bias_s[kMaxExperts];
   __shared__ int4 scratch[8];
   __shared__ unsigned last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < kMaxExperts; i += blockDim.x) hist[i] = 0;
+  for (int i = threadIdx.x; i < kMaxExperts; i += blockDim.x) {
+    hist[i] = 0;
+    bias_s[i] = i < d.E ? bias[i] : 0.f;
+  }
   __syncthreads();
-  const int t0 = blockIdx.x * kTopkTokens;
-  for (int t = t0 + warp; t < min(d.T, t0 + kTopkTokens); t += 8) {
+  // each warp ranks every 8th token of the CTA's range; the next token's
+  // logits are in flight while this one is ranked
+  const int t0 = blockIdx.x * kTopkTokens, t1 = min(d.T, t0 + kTopkTokens);
+  float nx[kPer];
+  if (t0 + warp < t1) load_row(r.logits + (size_t)(t0 + warp) * d.E, d.E, lane, nx);
+  for (int t = t0 + warp; t < t1; t += 8) {
+    float lg[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) lg[i] = nx[i];
+    if (t + 8 < t1) load_row(r.logits + (size_t)(t + 8) * d.E, d.E, lane, nx);
     int id;
     float w;
-    warp_topk(r.logits + (size_t)t * d.E, bias, d.E, d.k, lane, &id, &w);
+    warp_topk_regs(lg, bias_s, d.E, d.k, lane, &id, &w);
     if (lane < d.k) {
       if (id < 0 || id >= d.E) {
         atomicOr(r.err, kErrRange);
@@ -387,15 +422,36 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
   __threadfence();
   const int nblk = gridDim.x;
   const int e = threadIdx.x;
+  // the per-CTA counts, 8 loads in flight at a time
   int c = 0;
-  if (e < d.E)
-    for (int b = 0; b < nblk; ++b) c += __ldcg(r.blockcnt + (size_t)b * d.E + e);
+  if (e < d.E) {
+    int b = 0;
+    for (; b + 8 <= nblk; b += 8) {
+      int v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = __ldcg(r.blockcnt + (size_t)(b + q) * d.E + e);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) c += v[q];
+    }
+    for (; b < nblk; ++b) c += __ldcg(r.blockcnt + (size_t)b * d.E + e);
+  }
   if (e < kMaxExperts) counts_s[e] = c;
   __syncthreads();
   finish_counts(d, counts_s, offs_s, r, scratch);
   if (e < d.E) {
     int run = offs_s[e];
-    for (int b = 0; b < nblk; ++b) {
+    int b = 0;
+    for (; b + 8 <= nblk; b += 8) {
+      int v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = __ldcg(r.blockcnt + (size_t)(b + q) * d.E + e);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        r.blockbase[(size_t)(b + q) * d.E + e] = run;
+        run += v[q];
+      }
+    }
+    for (; b < nblk; ++b) {
       r.blockbase[(size_t)b * d.E + e] = run;
       run += __ldcg(r.blockcnt + (size_t)b * d.E + e);
     }
