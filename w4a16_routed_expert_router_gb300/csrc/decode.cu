@@ -39,8 +39,8 @@
 //    stage; it only ever waits for free stages, so the weight stream never
 //    stops on a dependency. A stage holds the weights plus room for the
 //    pass's activation rows (min(T, 8)), so a small batch gets more stages:
-//    at one token about 11 stages (176 KB of weights in flight per SM) instead
-//    of 5, enough to cover the ~1.5 us a weight box takes to arrive.
+//    at one token 9 stages (144 KB of weights in flight per SM) instead of 5
+//    at 64 tokens, enough to cover the ~1.5 us a weight box takes to arrive.
 //  * 1 activation warp: in ring order, copies each stage's activation rows
 //    (interleaved x for gate/up, h for down) into the stage (1-D bulk copies). Down tasks
 //    need the h rows of their (expert, pass): it polls the completion counters
