@@ -36,6 +36,24 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
+def _header_constants():
+    """Every MOE_W4A16_* value the header defines (#define or enum member)."""
+    text = open(HEADER).read()
+    vals = {}
+    for name, v in re.findall(r"#define\s+(MOE_W4A16_[A-Z0-9_]+)\s+(0x[0-9a-fA-F]+|\d+)u?\b", text):
+        vals[name] = int(v, 0)
+    for name, v in re.findall(r"\b(MOE_W4A16_[A-Z0-9_]+)\s*=\s*(-?\d+)", text):
+        vals[name] = int(v)
+    return vals
+
+
+def test_binding_constants_match_the_header():
+    vals = _header_constants()
+    assert "MOE_W4A16_ERR_NO_DEVICE" in vals and "MOE_W4A16_DEVERR_LAYOUT" in vals
+    for name, v in vals.items():
+        assert getattr(moe, name, None) == v, name
+
+
 def test_status_strings(L):
     assert moe.moe_w4a16_status_string(0) == "ok"
     assert "max_tokens" in moe.moe_w4a16_status_string(moe.MOE_W4A16_ERR_TOO_MANY_TOKENS)

@@ -26,6 +26,11 @@ MOE_W4A16_FLAG_FORCE_GEMV = 0x1
 MOE_W4A16_FLAG_FORCE_TC = 0x2
 MOE_W4A16_FLAG_PROFILE = 0x4
 
+# device error flag bits (moe_w4a16_check_device_errors)
+MOE_W4A16_DEVERR_TIMEOUT = 0x1
+MOE_W4A16_DEVERR_RANGE = 0x2
+MOE_W4A16_DEVERR_LAYOUT = 0x4
+
 # every symbol include/moe_w4a16.h declares
 EXPORTS = (
     "moe_w4a16_workspace_bytes",
