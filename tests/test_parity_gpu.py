@@ -84,6 +84,28 @@ def test_odd_shape_parity(odd, T):
     obj.close()
 
 
+# a layer without a shared expert (shared_inter = 0): the decode kernel, the
+# tensor-core path and the GEMV engine
+@pytest.fixture(scope="module")
+def noshared():
+    shape = ms.MoeShape("noshared", 16, 256, 8, 2, 128, 0, 1007, 1007)
+    tensors = upload_layer(mc.weights_of(shape), DEV)[0]
+    return shape, tensors
+
+
+@pytest.mark.parametrize("flags,T", [(0, 1), (0, 16), (0, 64), (0, 65), (0, 200),
+                                     (moe.MOE_W4A16_FLAG_FORCE_GEMV, 100)])
+def test_no_shared_expert_parity(noshared, flags, T):
+    shape, tensors = noshared
+    layer = mc.layer_with_tokens(shape, T)
+    ref = mc.oracle(layer)
+    obj = _layer_obj(layer, tensors, max_tokens=256, flags=flags)
+    out, rt = _run(obj, layer.x)
+    mc.check_routing(rt, ref, shape.experts)
+    mc.check_output(out, ref["out"])
+    obj.close()
+
+
 @pytest.mark.parametrize("flags,T", [
     (moe.MOE_W4A16_FLAG_FORCE_TC, 1), (moe.MOE_W4A16_FLAG_FORCE_TC, 16),
     (moe.MOE_W4A16_FLAG_FORCE_TC, 64), (moe.MOE_W4A16_FLAG_FORCE_TC, 300),
