@@ -91,8 +91,9 @@ def kernel_work(name, shape, work):
     if name.startswith("gemv_gate_up"):
         return work["w13_bytes"] + T * H * 2 + hrows * 2, f13
     if name.startswith("tc_gate_up"):
-        # x gathered into expert order is read once more by the GEMM
-        return work["w13_bytes"] + rows * H * 2 + hrows * 2, f13
+        # activations counted once (T rows); the expert-ordered copy of x the
+        # GEMM reads instead is an implementation choice (implementation_bytes)
+        return work["w13_bytes"] + T * H * 2 + hrows * 2, f13
     if name.startswith("gemv_down") or name.startswith("tc_down"):
         return work["w2_bytes"] + hrows * 2 + rows * H * 4, f2
     if name.startswith("route") or name.startswith("router"):
@@ -102,21 +103,34 @@ def kernel_work(name, shape, work):
     return 0, 0
 
 
+def implementation_bytes(name, shape):
+    """DRAM bytes a kernel moves beyond its algorithmic ones by design (not
+    counted in the roofline): the tensor-core gate/up GEMM reads x gathered
+    into expert order (T*k + T rows) instead of the T token rows."""
+    if name.startswith("tc_gate_up"):
+        rows = shape.tokens * shape.top_k + (shape.tokens if shape.shared_inter else 0)
+        return (rows - shape.tokens) * shape.hidden * 2
+    return 0
+
+
 def roofline(name, shape, work, seconds, pk):
     """Roofline entry of one kernel: whichever of the HBM and bf16 tensor
     bounds is slower for its algorithmic work decides the bound."""
     nbytes, flops = kernel_work(name, shape, work)
+    extra = implementation_bytes(name, shape)
     t_mem = nbytes / (pk["hbm_gbs"] * 1e9)
     t_mma = flops / (pk["bf16_tflops"] * 1e12)
     if t_mma > t_mem:
         ach = flops / seconds / 1e12
         return {"kernel": name, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "algorithmic_flops": flops,
-                "algorithmic_bytes": nbytes, "peak_source": pk["source"] + " (burst)"}
+                "algorithmic_bytes": nbytes, "implementation_bytes": extra,
+                "peak_source": pk["source"] + " (burst)"}
     ach = nbytes / seconds / 1e9
     return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
             "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "algorithmic_bytes": nbytes,
-            "algorithmic_flops": flops, "peak_source": pk["source"]}
+            "algorithmic_flops": flops, "implementation_bytes": extra,
+            "peak_source": pk["source"]}
 
 
 # ------------------------------------------------------------------- clocks
@@ -251,6 +265,17 @@ def oracle_sample(shape, budget_s=15.0):
             "cores": max(1, round(cpu / wall)) if wall > 0 else 1}
 
 
+def config_of(shape, args):
+    """The workload description both arms print (the same dict, so that the
+    two lines can be compared key by key)."""
+    return {"workload": shape.name, "tokens": shape.tokens, "hidden": shape.hidden,
+            "experts": shape.experts, "top_k": shape.top_k, "inter": shape.inter,
+            "shared_inter": shape.shared_inter, "weights": "int4 g128 symmetric",
+            "l2": "flushed before every step (512 MB read, untimed)",
+            "graph": "one forward per CUDA-graph replay", "parallelism": "replicas",
+            "expert_path": args.expert_path}
+
+
 def run_reference(args, shape):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -264,9 +289,7 @@ def run_reference(args, shape):
             "warmup": args.warmup, "ms_per_step": 1000.0 * r["wall_s"] / max(r["tokens"], 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": shape.name, "tokens": shape.tokens, "hidden": shape.hidden,
-                       "experts": shape.experts, "top_k": shape.top_k, "inter": shape.inter,
-                       "shared_inter": shape.shared_inter},
+            "config": config_of(shape, args),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": r["cores"],
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -275,11 +298,170 @@ def run_reference(args, shape):
 
 
 # --------------------------------------------------------------- GPU arm
+class Bench:
+    """One device, one uploaded copy of each distinct layer's weights; measures
+    workloads on it."""
+
+    def __init__(self, args, dev, dist):
+        import torch
+        self.torch = torch
+        self.args = args
+        self.dev = dev
+        self.dist = dist
+        self.layers = {}
+        # L2 flush: reading a 512 MB buffer (4x the 129 MB L2) leaves only
+        # clean lines of that buffer in L2, so the timed step starts cold and
+        # pays no write-back of someone else's dirty lines.
+        self.flush = torch.ones(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        self.flush_out = torch.empty((), dtype=torch.float32, device=dev)
+        self.stream = torch.cuda.Stream(device=dev)
+
+    def flush_l2(self):
+        self.torch.sum(self.flush, dim=0, out=self.flush_out)
+
+    def tensors(self, shape):
+        from moe_synth.device import upload_layer
+        key = (shape.layer_seed, shape.hidden, shape.experts, shape.inter, shape.shared_inter)
+        if key not in self.layers:
+            base = ms.make_layer(shape.with_tokens(0), x=np.zeros((0, shape.hidden), np.uint16))
+            self.layers[key] = upload_layer(base, self.dev)[0]
+        t = dict(self.layers[key])
+        t["router_bias"] = self.torch.from_numpy(ms.router_bias(shape)).to(self.dev)
+        return t
+
+    def measure(self, shape, steps, warmup, clocks):
+        """Time one workload: CUDA-graph replays (L2 flushed before each), the
+        per-kernel durations, and the host-buffer entry point end to end."""
+        import w4a16_routed_expert_router_gb300 as moe
+        from moe_synth.device import upload_tokens
+        torch, dev, dist, stream = self.torch, self.dev, self.dist, self.stream
+        tensors = self.tensors(shape)
+        T, H = shape.tokens, shape.hidden
+        # distinct token batches (same distribution), resident in HBM before timing
+        nx = min(steps, 8)
+        xs = [upload_tokens(ms.tokens(dataclasses.replace(shape, token_seed=shape.token_seed + 7919 * i)),
+                            dev) for i in range(nx)]
+        out = torch.empty((T, H), dtype=torch.int16, device=dev)
+        path_flags = {"auto": 0, "tc": moe.MOE_W4A16_FLAG_FORCE_TC,
+                      "gemv": moe.MOE_W4A16_FLAG_FORCE_GEMV}[self.args.expert_path]
+        obj = moe.MoeLayer(shape.hidden, shape.experts, shape.top_k, shape.inter,
+                           shape.shared_inter, T, tensors, flags=path_flags)
+        prof = moe.MoeLayer(shape.hidden, shape.experts, shape.top_k, shape.inter,
+                            shape.shared_inter, T, tensors,
+                            flags=path_flags | moe.MOE_W4A16_FLAG_PROFILE)
+        xin = torch.empty_like(xs[0])
+
+        # --- capture one forward in a CUDA graph (input copied into xin first)
+        with torch.cuda.stream(stream):
+            xin.copy_(xs[0])
+            obj.forward(xin, out, stream=stream)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            obj.forward(xin, out, stream=torch.cuda.current_stream())
+        launches_per_fwd = len(moe.moe_w4a16_last_launches(obj.handle))
+
+        def step(i, timed, ev=None):
+            with torch.cuda.stream(stream):
+                self.flush_l2()
+                xin.copy_(xs[i % nx])
+                if timed:
+                    ev[0].record(stream)
+                graph.replay()
+                if timed:
+                    ev[1].record(stream)
+
+        for i in range(warmup):
+            step(i, False)
+        stream.synchronize()
+        assert moe.moe_w4a16_check_device_errors(obj.handle) == 0
+
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with clocks:
+            for i in range(steps):
+                step(i, True, evs[i])
+            torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        total_ms = sum(a.elapsed_time(b) for a, b in evs)
+        total_ms = max_over_ranks(total_ms, dist, dev)
+        world = dist.get_world_size() if dist is not None else 1
+        ms_per_step = total_ms / steps
+        value = world * T * steps / (total_ms / 1000.0)
+
+        # --- routing stats of the timed inputs (for the algorithmic bytes)
+        rt_counts = []
+        for i in range(nx):
+            with torch.cuda.stream(stream):
+                obj.forward(xs[i], out, stream=stream)
+            stream.synchronize()
+            rt_counts.append(np.diff(obj.routing(T, stream=stream)["offsets"]))
+        works = [layer_work(shape, c) for c in rt_counts]
+        work = {k_: float(np.mean([w[k_] for w in works])) for k_ in works[0]}
+
+        # --- per-kernel durations with CUDA events (no graph), same flush
+        kernel_ms = {}
+        nprof = min(steps, 50)
+        for i in range(warmup + nprof):
+            with torch.cuda.stream(stream):
+                self.flush_l2()
+                prof.forward(xs[i % nx], out, stream=stream)
+            stream.synchronize()
+            if i >= warmup:
+                for name, t_ms in moe.moe_w4a16_last_launches(prof.handle):
+                    kernel_ms.setdefault(name, []).append(t_ms)
+        kernel_avg = {n: float(np.mean(v)) for n, v in kernel_ms.items()}
+        dominant = max(kernel_avg, key=kernel_avg.get)
+
+        # --- end to end through the host-buffer entry point
+        xh = torch.from_numpy(ms.tokens(shape).view(np.int16)).pin_memory()
+        oh = torch.empty((T, H), dtype=torch.int16).pin_memory()
+        for _ in range(3):
+            obj.forward_host(xh, oh, stream=stream)
+        e2e_s = 0.0
+        n_e2e = min(steps, 100)
+        for i in range(n_e2e):
+            with torch.cuda.stream(stream):
+                self.flush_l2()
+            stream.synchronize()
+            t0 = time.perf_counter()
+            obj.forward_host(xh, oh, stream=stream)
+            e2e_s += time.perf_counter() - t0
+        e2e_s = max_over_ranks(e2e_s, dist, dev)
+        e2e_value = world * T * n_e2e / e2e_s
+        assert moe.moe_w4a16_check_device_errors(obj.handle) == 0
+        obj.close()
+        prof.close()
+
+        pk = peaks()
+        roof = roofline(dominant, shape, work, kernel_avg[dominant] / 1000.0, pk)
+        roof["traffic"] = profiled_traffic(dominant, shape.name)
+        layer_roof_s = max(work["bytes"] / (pk["hbm_gbs"] * 1e9),
+                           work["flops"] / (pk["bf16_tflops"] * 1e12))
+        return {
+            "value": value, "unit": "tokens/s", "ms_per_step": ms_per_step, "steps": steps,
+            "weight_stream_gbs": work["weight_bytes"] / (ms_per_step / 1000.0) / 1e9,
+            "layer_roofline_frac": layer_roof_s / (ms_per_step / 1000.0),
+            "layer_bound": "tensor" if work["flops"] / (pk["bf16_tflops"] * 1e12) >
+                           work["bytes"] / (pk["hbm_gbs"] * 1e9) else "hbm",
+            "algorithmic_bytes": work["bytes"], "algorithmic_flops": work["flops"],
+            "experts_hit": work["hit"],
+            "roofline": roof,
+            "kernels_ms": kernel_avg,
+            "gpu_launches": launches_per_fwd * steps,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
+                    "d2h_bytes_per_step": T * H * 2},
+        }
+
+
 def run_ours(args, shape):
     import torch
 
     import w4a16_routed_expert_router_gb300 as moe
-    from moe_synth.device import upload_layer, upload_tokens
     from w4a16_routed_expert_router_gb300 import _build
 
     world, rank, local = dist_env()
@@ -292,155 +474,41 @@ def run_ours(args, shape):
         dist.barrier()
     moe.lib()
 
-    layer = ms.make_layer(shape)          # weights + tokens (unguarded draw)
-    tensors = upload_layer(layer, dev)[0]
-    T, H = shape.tokens, shape.hidden
-    steps = args.steps
-    # distinct token batches (same distribution), resident in HBM before timing
-    nx = min(steps, 8)
-    xs = [upload_tokens(ms.tokens(dataclasses.replace(shape, token_seed=shape.token_seed + 7919 * i)),
-                        dev) for i in range(nx)]
-    out = torch.empty((T, H), dtype=torch.int16, device=dev)
-    # L2 flush: reading a 512 MB buffer (4x the 129 MB L2) leaves only clean
-    # lines of that buffer in L2, so the timed step starts cold and pays no
-    # write-back of someone else's dirty lines.
-    flush = torch.ones(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    flush_out = torch.empty((), dtype=torch.float32, device=dev)
-
-    def flush_l2():
-        torch.sum(flush, dim=0, out=flush_out)
-
-    path_flags = {"auto": 0, "tc": moe.MOE_W4A16_FLAG_FORCE_TC,
-                  "gemv": moe.MOE_W4A16_FLAG_FORCE_GEMV}[args.expert_path]
-    obj = moe.MoeLayer(shape.hidden, shape.experts, shape.top_k, shape.inter,
-                       shape.shared_inter, T, tensors, flags=path_flags)
-    prof = moe.MoeLayer(shape.hidden, shape.experts, shape.top_k, shape.inter,
-                        shape.shared_inter, T, tensors,
-                        flags=path_flags | moe.MOE_W4A16_FLAG_PROFILE)
-    stream = torch.cuda.Stream(device=dev)
-    xin = torch.empty_like(xs[0])
-
-    # --- capture one forward in a CUDA graph (input copied into xin first)
-    with torch.cuda.stream(stream):
-        xin.copy_(xs[0])
-        obj.forward(xin, out, stream=stream)
-    stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        obj.forward(xin, out, stream=torch.cuda.current_stream())
-    launches_per_fwd = len(moe.moe_w4a16_last_launches(obj.handle))
-
-    def step(i, timed, ev=None):
-        with torch.cuda.stream(stream):
-            flush_l2()
-            xin.copy_(xs[i % nx])
-            if timed:
-                ev[0].record(stream)
-            graph.replay()
-            if timed:
-                ev[1].record(stream)
-
-    for i in range(args.warmup):
-        step(i, False)
-    stream.synchronize()
-    assert moe.moe_w4a16_check_device_errors(obj.handle) == 0
-
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        for i in range(steps):
-            step(i, True, evs[i])
-        torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    per_step = [a.elapsed_time(b) for a, b in evs]
-    total_ms = sum(per_step)
-    total_ms = max_over_ranks(total_ms, dist, dev)
-    ms_per_step = total_ms / steps
-    value = world * T * steps / (total_ms / 1000.0)
-
-    # --- routing stats of the timed inputs (for the algorithmic bytes)
-    rt_counts = []
-    for i in range(nx):
-        with torch.cuda.stream(stream):
-            obj.forward(xs[i], out, stream=stream)
-        stream.synchronize()
-        rt_counts.append(np.diff(obj.routing(T, stream=stream)["offsets"]))
-    works = [layer_work(shape, c) for c in rt_counts]
-    work = {k_: float(np.mean([w[k_] for w in works])) for k_ in works[0]}
-
-    # --- per-kernel durations with CUDA events (no graph), same flush
-    kernel_ms = {}
-    nprof = min(steps, 50)
-    for i in range(args.warmup + nprof):
-        with torch.cuda.stream(stream):
-            flush_l2()
-            prof.forward(xs[i % nx], out, stream=stream)
-        stream.synchronize()
-        if i >= args.warmup:
-            for name, t_ms in moe.moe_w4a16_last_launches(prof.handle):
-                kernel_ms.setdefault(name, []).append(t_ms)
-    kernel_avg = {n: float(np.mean(v)) for n, v in kernel_ms.items()}
-    dominant = max(kernel_avg, key=kernel_avg.get)
-
-    # --- end to end through the host-buffer entry point
-    xh = torch.from_numpy(ms.tokens(shape).view(np.int16)).pin_memory()
-    oh = torch.empty((T, H), dtype=torch.int16).pin_memory()
-    for _ in range(3):
-        obj.forward_host(xh, oh, stream=stream)
-    e2e_s = 0.0
-    n_e2e = min(steps, 100)
-    for i in range(n_e2e):
-        with torch.cuda.stream(stream):
-            flush_l2()
-        stream.synchronize()
-        t0 = time.perf_counter()
-        obj.forward_host(xh, oh, stream=stream)
-        e2e_s += time.perf_counter() - t0
-    e2e_s = max_over_ranks(e2e_s, dist, dev)
-    e2e_value = world * T * n_e2e / e2e_s
-
-    pk = peaks()
-    roof = roofline(dominant, shape, work, kernel_avg[dominant] / 1000.0, pk)
-    roof["traffic"] = profiled_traffic(dominant, shape.name)
-    layer_roof_s = max(work["bytes"] / (pk["hbm_gbs"] * 1e9),
-                       work["flops"] / (pk["bf16_tflops"] * 1e12))
+    b = Bench(args, dev, dist)
+    clocks = ClockSampler(local)
+    head = b.measure(shape, args.steps, args.warmup, clocks)
     clk = clocks.summary()
+    others = {}
+    for name in args.per_config:
+        if name == shape.name:
+            continue
+        c = ClockSampler(local)
+        r = b.measure(ms.CONFIGS[name], min(args.steps, 100), args.warmup, c)
+        r["clocks"] = c.summary()
+        others[name] = r
 
     if rank == 0:
         cpu = oracle_sample(shape, budget_s=15.0) if world == 1 else None
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s",
-            "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "metric": METRIC, "value": head["value"], "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": head["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": shape.name, "tokens": T, "hidden": H,
-                       "experts": shape.experts, "top_k": shape.top_k, "inter": shape.inter,
-                       "shared_inter": shape.shared_inter, "weights": "int4 g128 symmetric",
-                       "l2": "flushed before every step (512 MB read, untimed)",
-                       "graph": "one forward per CUDA-graph replay", "parallelism": "replicas",
-                       "expert_path": args.expert_path},
-            "weight_stream_gbs": work["weight_bytes"] / (ms_per_step / 1000.0) / 1e9,
-            "layer_roofline_frac": layer_roof_s / (ms_per_step / 1000.0),
-            "experts_hit": work["hit"],
-            "roofline": roof,
-            "kernels_ms": kernel_avg,
-            "gpu_launches": launches_per_fwd * steps,
-            "clocks": clk,
-            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
-                    "d2h_bytes_per_step": T * H * 2},
+            "config": config_of(shape, args),
         }
+        for k_ in ("weight_stream_gbs", "layer_roofline_frac", "layer_bound", "experts_hit",
+                   "roofline", "kernels_ms", "gpu_launches", "e2e"):
+            line[k_] = head[k_]
+        line["clocks"] = clk
         if cpu is not None:
             line["cpu_baseline"] = {"value": cpu["tokens"] / cpu["wall_s"], "unit": "tokens/s",
                                     "cores": cpu["cores"], "kind": "oracle",
                                     "sample": f"{cpu['tokens']} tokens of {shape.name} batches "
                                               f"({cpu['wall_s']:.1f} s wall)"}
+        if others:
+            line["per_config"] = others
         print(json.dumps(line), flush=True)
-    obj.close()
-    prof.close()
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -455,7 +523,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--expert-path", default="auto", choices=["auto", "tc", "gemv"],
                     help="expert kernels: the library's choice, tensor-core, or split-K GEMV")
+    ap.add_argument("--per-config", default="decode64,prefill8192,zipf2048",
+                    help="further workloads measured after the headline one and reported "
+                         "under per_config (comma-separated; 'none' for none)")
     args = ap.parse_args()
+    args.per_config = [] if args.per_config in ("", "none") else args.per_config.split(",")
+    for name in args.per_config:
+        if name not in ms.CONFIGS:
+            ap.error(f"unknown workload {name}")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     shape = ms.CONFIGS[args.config]

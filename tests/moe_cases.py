@@ -85,3 +85,79 @@ def check_routing(gpu: dict, ref: dict, E: int):
     np.testing.assert_array_equal(gpu["inv"], ref["inv"])
     np.testing.assert_allclose(gpu["weights"], ref["weights"], rtol=2e-6, atol=1e-7)
     assert gpu["offsets"][-1] == ref["ids"].size
+
+
+# ---------------------------------------------------- full-size output checks
+def covering_tokens(route: dict, tile_rows: int = 256) -> np.ndarray:
+    """Tokens whose outputs touch every active expert's segment at both ends.
+
+    For each expert with rows: the token of its first and of its last row,
+    and for segments longer than ``tile_rows`` (the row tile of the
+    tensor-core experts) the first and last row of every tile. Every routed
+    expert's weights, every row tile boundary and (since whole output rows are
+    compared) every output channel tile are then checked against the oracle.
+    """
+    perm, offsets = route["perm"], route["offsets"]
+    picks = {0, int(route["ids"].shape[0]) - 1}
+    for e in range(offsets.size - 1):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        for r0 in range(a, b, tile_rows):
+            r1 = min(b, r0 + tile_rows) - 1
+            picks.add(int(perm[r0]))
+            picks.add(int(perm[r1]))
+    return np.array(sorted(p for p in picks if p >= 0), dtype=np.int64)
+
+
+def _expert_rows_worker(args):
+    """One expert's SwiGLU output for some token rows, in a pool worker.
+
+    The expert's weights are drawn again from the layer's seeds (the same
+    generator as the layer under test), then dequantised and applied with the
+    oracle's own functions.
+    """
+    shape, e, x_bits = args
+    w13, w2 = mo.expert_dense(ms.expert_weights(shape, e), shape.group)
+    return e, mo.swiglu_expert(mo.bf16_to_f64(x_bits), w13, w2)
+
+
+def oracle_outputs(layer: ms.LayerInputs, route: dict, subset, workers: int = 0) -> np.ndarray:
+    """``mo.moe_forward(...)["out"]`` for ``subset``, with the experts spread over
+    a pool of spawned processes.
+
+    The per-expert SwiGLU outputs come from the oracle's functions, and they
+    are added up in the order ``moe_forward`` uses (the shared expert, then the
+    routed experts in ascending index), so the result equals ``moe_forward``'s
+    to fp64 rounding (a CPU test checks that). ``route`` is the oracle's routing of
+    the whole batch. The weights must be the ones the shape's seeds draw.
+    """
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    import os
+
+    shape = layer.shape
+    subset = np.asarray(subset, dtype=np.int64)
+    xs = layer.x[subset]
+    ids = route["ids"][subset]
+    wts = route["weights"][subset]
+    experts = [int(e) for e in np.unique(ids)]
+    jobs = []
+    if shape.shared_inter:
+        jobs.append((shape, shape.experts, xs))
+    for e in experts:
+        rows, _ = np.nonzero(ids == e)
+        jobs.append((shape, e, xs[rows]))
+    n = workers or min(16, os.cpu_count() or 1)
+    if n > 1 and len(jobs) > 1:
+        # spawned workers (never forked after CUDA is up); a worker that dies
+        # raises in the caller instead of stalling the pool
+        with cf.ProcessPoolExecutor(n, mp_context=mp.get_context("spawn")) as pool:
+            ys = dict(pool.map(_expert_rows_worker, jobs))
+    else:
+        ys = dict(map(_expert_rows_worker, jobs))
+    out = np.zeros((subset.size, shape.hidden))
+    if shape.shared_inter:
+        out += ys[shape.experts]
+    for e in experts:
+        rows, slots = np.nonzero(ids == e)
+        out[rows] += wts[rows, slots][:, None] * ys[e]
+    return out

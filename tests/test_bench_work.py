@@ -75,3 +75,23 @@ def test_roofline_takes_the_slower_bound():
     r = bench.roofline("tc_gate_up_swiglu", p, wp, 1.38e-3, MEASURED)
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
     assert abs(r["frac"] - r["achieved"] / 1885.7) < 1e-12
+
+
+def test_tensor_core_gate_up_counts_activations_once():
+    # the layer reads each token row once; the gathered copy the GEMM reads
+    # (T*k + T rows) is reported apart, not as algorithmic bytes
+    shape = ms.CONFIGS["prefill8192"]
+    work = bench.layer_work(shape, np.full(shape.experts, 192))
+    nbytes, _ = bench.kernel_work("tc_gate_up_swiglu", shape, work)
+    hrows = 8192 * 6 * 2048 + 8192 * 2048
+    assert nbytes == work["w13_bytes"] + 8192 * 4096 * 2 + hrows * 2
+    assert bench.implementation_bytes("tc_gate_up_swiglu", shape) == 8192 * 6 * 4096 * 2
+    assert bench.implementation_bytes("decode_fused", shape) == 0
+
+
+def test_both_arms_print_the_same_config():
+    import argparse
+    args = argparse.Namespace(expert_path="auto")
+    shape = ms.CONFIGS["decode1"]
+    c = bench.config_of(shape, args)
+    assert c["workload"] == "decode1" and c["tokens"] == 1 and c["experts"] == 256

@@ -323,3 +323,74 @@ def test_zipf_bias_gives_zipf_popularity_on_workload_tokens():
     r = np.arange(2, 41)
     slope = np.polyfit(np.log(r), np.log(counts[1:40]), 1)[0]
     assert -1.35 < slope < -0.85, slope
+
+
+# ------------------------------------------------------------ selection margin
+def test_selection_margin_closed_form_with_bias():
+    # logits (ln 3, 0, -ln 3, 0) give s = (3/4, 1/2, 1/4, 1/2); with the bias
+    # (0, 0.4, 0.6875, 0.125) the selection scores are (0.75, 0.9, 0.9375, 0.625):
+    # sorted 0.9375 > 0.9 > 0.75 > 0.625, so k = 1, 2, 3 give the gaps 0.0375,
+    # 0.15 and 0.125. Without the bias (s alone: 0.75, 0.5, 0.5, 0.25) they
+    # would be 0.25, 0 and 0.25; with k off by one they would be permuted.
+    logits = np.array([[math.log(3.0), 0.0, -math.log(3.0), 0.0]])
+    bias = np.array([0.0, 0.4, 0.6875, 0.125], dtype=np.float32)
+    want = {1: 0.0375, 2: 0.15, 3: 0.125}
+    for k, g in want.items():
+        got = mo.selection_margin(logits, bias, k)
+        assert got.shape == (1,)
+        # 0.4 is not exact in fp32 (0.4 + 6e-9)
+        assert abs(got[0] - g) < 1e-7, (k, got)
+
+
+def test_selection_margin_distinct_gaps_locate_k():
+    # selection scores whose consecutive gaps are all different: 0.9, 0.8,
+    # 0.55, 0.5 (logits 0, so s = 1/2, plus a bias); the k-th/(k+1)-th gap is
+    # 0.1 for k = 1, 0.25 for k = 2 and 0.05 for k = 3, so an off-by-one in k
+    # or a swapped pair cannot pass
+    bias = np.array([0.05, 0.3, 0.4, 0.0], dtype=np.float32)  # sel 0.55 0.8 0.9 0.5
+    logits = np.zeros((1, 4))
+    want = {1: 0.1, 2: 0.25, 3: 0.05}
+    for k, g in want.items():
+        np.testing.assert_allclose(mo.selection_margin(logits, bias, k), [g], rtol=0, atol=1e-7)
+
+
+def test_selection_margin_brute_force_and_topk_boundary():
+    # random rows: the margin equals the gap between the k-th and (k+1)-th
+    # value of a plain Python sort of sigmoid(logit) + bias, and it is the
+    # smallest chosen selection score minus the largest unchosen one
+    rng = np.random.default_rng(17)
+    T, E, k = 50, 12, 3
+    logits = rng.standard_normal((T, E)) * 2
+    bias = (rng.standard_normal(E) * 0.2).astype(np.float32)
+    m = mo.selection_margin(logits, bias, k)
+    ids, _, sel = mo.select_topk(logits, bias, k)
+    for t in range(T):
+        vals = sorted((1.0 / (1.0 + math.exp(-float(logits[t, e]))) + float(bias[e])
+                       for e in range(E)), reverse=True)
+        assert abs(m[t] - (vals[k - 1] - vals[k])) < 1e-14
+        chosen = [sel[t, e] for e in ids[t]]
+        rest = [sel[t, e] for e in range(E) if e not in set(ids[t])]
+        assert abs(m[t] - (min(chosen) - max(rest))) < 1e-15
+        assert m[t] >= 0.0
+
+
+def test_selection_margin_zero_on_a_tie():
+    # two experts tie for the k-th place: the margin is exactly 0, which the
+    # input guard (margin < 1e-3) rejects
+    logits = np.array([[1.0, 0.5, 0.5, -1.0]])
+    np.testing.assert_array_equal(mo.selection_margin(logits, np.zeros(4, np.float32), 2), [0.0])
+
+
+# ------------------------------------------------ test helper on the oracle
+def test_parallel_oracle_outputs_equal_moe_forward(tiny):
+    from tests import moe_cases as mc
+    r = _fwd(tiny)
+    subset = mc.covering_tokens(r, tile_rows=3)
+    assert subset.size >= 4
+    # every routed expert with rows appears among the covering tokens
+    got_e = set(np.unique(r["ids"][subset]).tolist())
+    assert got_e == set(np.nonzero(r["counts"])[0].tolist())
+    want = _fwd(tiny, subset=subset)["out"]
+    for workers in (1, 2):
+        out = mc.oracle_outputs(tiny, r, subset, workers=workers)
+        np.testing.assert_allclose(out, want, rtol=1e-12, atol=1e-15)

@@ -384,11 +384,13 @@ int moe_w4a16_create(const moe_w4a16_config* cfg, int device, moe_w4a16_handle**
     delete h;
     return st;
   }
-  if ((st = cuda_status(tc_setup(&tc_per_sm))) != MOE_W4A16_OK || tc_per_sm < 1) {
+  // the tensor-core experts keep all of an SM's TMEM per CTA: exactly one
+  // resident CTA per SM, one persistent CTA per SM in the grid
+  if ((st = cuda_status(tc_setup(&tc_per_sm))) != MOE_W4A16_OK || tc_per_sm != 1) {
     delete h;
     return st != MOE_W4A16_OK ? st : MOE_W4A16_ERR_CUDA;
   }
-  h->tc_grid = h->num_sms * tc_per_sm;
+  h->tc_grid = h->num_sms;
 
   const Layout L = plan(*cfg);
   if ((st = cuda_status(cudaMalloc(&h->ws, L.total))) != MOE_W4A16_OK) {

@@ -44,6 +44,9 @@ struct RSmem {
   uint32_t tmem_base;
 };
 constexpr int kRSmemBytes = (int)sizeof(RSmem) + 1024;
+// Each CTA allocates 256 of the SM's 512 TMEM columns: at most two CTAs may
+// share an SM, which the shared-memory footprint guarantees.
+static_assert(3 * kRSmemBytes > 228 * 1024, "router_tc_kernel must stay at <= 2 CTAs per SM");
 
 __global__ void __launch_bounds__(256) router_split_kernel(const float4* __restrict__ w,
                                                            uint2* __restrict__ planes, long long n4) {

@@ -84,6 +84,11 @@ struct Smem {
   uint32_t tmem_base;
 };
 constexpr int kSmemBytes = (int)sizeof(Smem) + 1024;  // + alignment slack
+// A CTA holds all 512 TMEM columns for its whole life, so a second CTA on the
+// same SM would wait in tcgen05.alloc until the first one exits. The shared-
+// memory footprint keeps the kernel at one CTA per SM (228 KB of shared memory
+// per SM), and the host refuses a launch shape with more.
+static_assert(2 * kSmemBytes > 228 * 1024, "tc_gemm_kernel must stay at one CTA per SM");
 
 struct TcParams {
   Dims d;
