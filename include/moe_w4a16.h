@@ -109,19 +109,32 @@ typedef struct moe_w4a16_weights {
 
 typedef struct moe_w4a16_handle moe_w4a16_handle;
 
-/* Bytes of device workspace a handle with this config allocates. */
+/* Bytes of device workspace a handle with this config allocates.
+ * No passage defines it: a sizing query of this library. */
 int moe_w4a16_workspace_bytes(const moe_w4a16_config* cfg, size_t* bytes);
 
 /* Validate cfg, bind to `device` (must be compute capability 10.3), allocate
- * the workspace and return a handle in *out. Synchronous. */
+ * the workspace and return a handle in *out. Synchronous.
+ * The sizes it accepts are the layer of "What does everyone get wrong about
+ * optimizing DeepSeek V4 Flash ...", section "Sparse architecture" (256
+ * routed + 1 shared expert, top-6) and "canada-quant/DeepSeek-V4-Flash-W4A16-
+ * FP8-MTP", table "Base model" (hidden 4096), generalised to any sizes in the
+ * ranges of moe_w4a16_config; group_size 128 is the card's "Component
+ * precisions" table. */
 int moe_w4a16_create(const moe_w4a16_config* cfg, int device, moe_w4a16_handle** out);
 
-/* Free the workspace and the handle (synchronises the device). NULL is OK. */
+/* Free the workspace and the handle (synchronises the device). NULL is OK.
+ * No passage defines it: resource release. */
 int moe_w4a16_destroy(moe_w4a16_handle* h);
 
 /* One forward pass on `stream` (a cudaStream_t; NULL = legacy default
- * stream). x and out are device pointers to bf16 [num_tokens, H]; out may
- * not alias x. Asynchronous: nothing is synchronised, and the call can be
+ * stream): the whole layer as written at the top of this header, i.e. the MoE
+ * FFN of "What does everyone get wrong ...", section "Sparse architecture",
+ * with the W4A16 experts of the model card's "Component precisions" table,
+ * run as weight-only kernels that turn the 4-bit weights into bf16 for bf16
+ * tensor cores ("Throughputmaxxing: DeepSeek-V4-Flash on Isambard-AI", "A pass
+ * through the model"). x and out are device pointers to bf16 [num_tokens, H];
+ * out may not alias x. Asynchronous: nothing is synchronised, and the call can be
  * captured into a CUDA graph (the weights struct is read on the host during
  * the call). num_tokens == 0 is a successful no-op. */
 int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t num_tokens,
@@ -129,7 +142,8 @@ int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t num_tokens
 
 /* The same forward with HOST activations: copies x_host (bf16 [T, H]) to the
  * device, runs the forward, copies the result to out_host and synchronises
- * `stream`. Host buffers should be pinned for asynchronous copies. With pinned
+ * `stream`. The computation is moe_w4a16_forward's; the host copies have no
+ * passage (an end-to-end convenience of this library). Host buffers should be pinned for asynchronous copies. With pinned
  * buffers (and without FLAG_PROFILE) the copy-forward-copy sequence is
  * recorded once into a CUDA graph owned by the handle and replayed while the
  * buffers, num_tokens and the weight pointers stay the same; a change records
@@ -138,7 +152,12 @@ int moe_w4a16_forward_host(moe_w4a16_handle* h, const uint16_t* x_host, int32_t 
                            const moe_w4a16_weights* w, uint16_t* out_host, void* stream);
 
 /* Copy the routing of the last forward into caller device buffers (any may be
- * NULL): topk_ids int32 [T, k], topk_w fp32 [T, k], offsets int32 [E + 1]
+ * NULL). The routing is the top-6 expert choice of "What does everyone get
+ * wrong ...", section "Sparse architecture", scored as the header's top
+ * comment states with the fp32 bias of the model card's "Component
+ * precisions" table; the offsets and permutation are the per-expert grouping
+ * of an indexed grouped GEMM ("Throughputmaxxing ...", "The Humming
+ * kernels"). Buffers: topk_ids int32 [T, k], topk_w fp32 [T, k], offsets int32 [E + 1]
  * (exclusive prefix of per-expert row counts), perm int32 [T*k] (token of
  * each expert-sorted row; rows of one expert in ascending token order), inv
  * int32 [T*k] (row of each (token, slot)). Asynchronous on `stream`. */
@@ -147,12 +166,16 @@ int moe_w4a16_get_routing(moe_w4a16_handle* h, int32_t* topk_ids, float* topk_w,
 
 /* Synchronise the handle's device, return the device error flag bits
  * (MOE_W4A16_DEVERR_*) in *flags and clear them. Returns
- * MOE_W4A16_ERR_DEVICE when any bit was set. */
+ * MOE_W4A16_ERR_DEVICE when any bit was set.
+ * No passage defines it: error reporting of this library. */
 int moe_w4a16_check_device_errors(moe_w4a16_handle* h, uint32_t* flags);
 
 /* Number of kernels the last forward launched, and (with FLAG_PROFILE) their
  * names and durations in milliseconds, read after the stream has finished.
- * names[i] points to static strings. Either array may be NULL. */
+ * names[i] points to static strings. Either array may be NULL.
+ * Measurement hook: the per-kernel breakdown follows "Throughputmaxxing ...",
+ * section "Where does the time go?" (time per kernel bucket against its
+ * roofline). */
 int moe_w4a16_last_launches(moe_w4a16_handle* h, int32_t* count, const char** names,
                             float* ms, int32_t capacity);
 
@@ -193,7 +216,7 @@ int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint16_t* x, in
  * multiple of 8, or a value outside [-8, 7]; nothing is written then. */
 int moe_w4a16_pack_int4(const int8_t* q, int64_t rows, int64_t K, uint32_t* out);
 
-/* Static description of a status code. */
+/* Static description of a status code. No passage defines it. */
 const char* moe_w4a16_status_string(int status);
 
 #ifdef __cplusplus
