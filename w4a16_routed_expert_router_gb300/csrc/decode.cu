@@ -250,13 +250,28 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, uin
       : "memory");
 }
 
-// A weight matrix whose rows are a whole number of 128-byte segments (K a
-// multiple of 256) is fetched as a 3-D box {32 words, 4 segments, 16 rows}
-// with the 128-byte swizzle: 16-byte chunk q of the 128-byte line at byte
-// offset o of the tile lands at chunk q ^ ((o >> 7) & 7). Rows 512 bytes apart
-// then differ in bit 2 of the swizzle, so the two rows read by a quarter warp
-// fall in opposite halves of the banks. Other matrices keep the plain 2-D box
-// (16 rows x 512 bytes, row-major).
+__device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
+                                       int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+// One TMA copy brings both 16-row weight tiles of a stage (8 K-groups each),
+// one more their group scales. A matrix whose rows are a whole number of
+// 128-byte segments (K a multiple of 256) is viewed in 128-byte segments and
+// fetched with the 128-byte swizzle: 16-byte chunk q of the 128-byte line at
+// byte offset o of the stage lands at chunk q ^ ((o >> 7) & 7). Rows 512 bytes
+// apart then differ in bit 2 of the swizzle, so the two rows read by a quarter
+// warp fall in opposite halves of the banks. Other matrices use plain
+// row-major boxes (512 bytes per row). Either way tile 0 sits in the first
+// 8 KB of the stage and tile 1 in the second, and the scales of tile 0 / 1 in
+// the first / second 256 bytes after them.
+//   gate/up (the gate rows of a tile and the up rows of the same channels,
+//   I' rows apart): a box over {row segment, segments, 16 rows, 2 halves};
+//   down (32 consecutive rows): a box over {row segment, segments, 32 rows}.
 __device__ __forceinline__ bool swizzled_k(int K) { return K % 256 == 0; }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
@@ -587,23 +602,8 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
     __threadfence();
     atomicAdd(&p.sync[0], 1u);
   }
-  // this CTA's share of the tokens (t = b, b + G, ...): the interleaved copy
-  // of x that every CTA's gate/up stages read; published on its own counter
-  {
-    const int h8 = d.H / 8;  // 16-byte chunks of a row; 16 per K group
-    for (int t = blockIdx.x; t < d.T; t += gridDim.x) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * d.H);
-      uint4* dst = reinterpret_cast<uint4*>(p.xi + (size_t)t * d.H);
-      for (int cidx = tid; cidx < h8; cidx += kRW * 32)
-        dst[(cidx & ~15) | chunk_t(cidx & 15)] = interleave8(__ldg(src + cidx));
-    }
-  }
   rbar();
   if (tid == 0) {
-    if ((int)blockIdx.x < d.T) {
-      __threadfence();
-      atomicAdd(&p.sync[1], 1u);
-    }
     s.flag = wait_counter(reinterpret_cast<const int*>(p.sync), (int)gridDim.x, p.r.err) ? 1 : 0;
   }
   for (int e = tid; e < kMaxExperts; e += kRW * 32) s.counts_s[e] = 0;
@@ -770,64 +770,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProd) {
     // ---------------------------------------------------------------- weight producer
-    bool known = false, stop = false;
-    int stage = 0;
-    uint32_t phase = 0;
+    // One lane decodes the CTA's tasks in order and fills the ring. Only the
+    // shared expert's gate/up tasks need no routing; the first routed task
+    // waits for this CTA's routing (shared memory).
     if (lane == 0) {
       prefetch_tmap(&tm13r);
       prefetch_tmap(&tm13s);
       prefetch_tmap(&tm2r);
       prefetch_tmap(&tm2s);
-    }
-    // Tasks are decoded 32 at a time, lane l taking the CTA's l-th next task,
-    // and handed out one by one by shuffles: the per-task decode (a search
-    // over the active experts, divisions) runs once per 32 tasks. A batch
-    // never spans the end of the routing-free part (the shared gate/up
-    // tasks), so that work never waits for the routing.
-    const int sh_end = cnt.sh1;
-    Task mine{};
-    int bi = 32;
-    for (int tau = blockIdx.x; !stop; tau += gridDim.x, ++bi) {
-      if (tau >= sh_end && !known) {
-        // routed tasks: wait for this CTA's routing (shared memory)
-        int ok = 1;
-        if (lane == 0) ok = dwait(&s.route_ready, 0, err) ? 1 : 0;
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        __syncwarp();  // orders every lane's routing reads after lane 0's wait
-        cnt.n_act = s.meta[0];
-        cnt.r1 = s.meta[1];
-        cnt.r2 = s.meta[2];
-        known = true;
-        bi = 32;  // the current batch (shared tasks) ends here
-      }
-      if (bi == 32) {
-        const int tl = tau + lane * (int)gridDim.x;
-        if ((tau < sh_end) == (tl < sh_end)) {
-          mine = task_at(s, d, cnt, tl);
-        } else {
-          mine = Task{};
-          mine.ngroups = 0;
+      bool known = false, stop = false;
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tau = blockIdx.x; !stop; tau += gridDim.x) {
+        if (tau >= cnt.sh1 && !known) {
+          if (!dwait(&s.route_ready, 0, err)) break;
+          cnt.n_act = s.meta[0];
+          cnt.r1 = s.meta[1];
+          cnt.r2 = s.meta[2];
+          known = true;
         }
-        bi = 0;
-      }
-      Task t;
-      t.down = __shfl_sync(0xffffffffu, mine.down ? 1 : 0, bi) != 0;
-      t.shared = __shfl_sync(0xffffffffu, mine.shared ? 1 : 0, bi) != 0;
-      t.e = __shfl_sync(0xffffffffu, mine.e, bi);
-      t.ngroups = __shfl_sync(0xffffffffu, mine.ngroups, bi);
-      t.rowA0 = __shfl_sync(0xffffffffu, mine.rowA0, bi);
-      t.rowA1 = __shfl_sync(0xffffffffu, mine.rowA1, bi);
-      t.r0 = __shfl_sync(0xffffffffu, mine.r0, bi);
-      t.nr = __shfl_sync(0xffffffffu, mine.nr, bi);
-      t.tile = __shfl_sync(0xffffffffu, mine.tile, bi);
-      t.pass = __shfl_sync(0xffffffffu, mine.pass, bi);
-      // past the last task (a batch that reached the end of the shared tasks
-      // was restarted above, where the routed range begins)
-      if (t.ngroups == 0) break;
-      if (lane == 0) {
+        const Task t = task_at(s, d, cnt, tau);
+        if (t.ngroups == 0) break;  // past the last task
         const CUtensorMap* tm = t.down ? (t.shared ? &tm2s : &tm2r) : (t.shared ? &tm13s : &tm13r);
         const CUtensorMap* ts = t.down ? (t.shared ? &ts2s : &ts2r) : (t.shared ? &ts13s : &ts13r);
         const bool swz = swizzled_k(t.ngroups * kGroup);
+        const int half = t.shared ? 0 : 2 * t.e;  // gate half of the expert (up: half + 1)
         for (int g0 = 0; g0 < t.ngroups; g0 += 8) {
           const int gcnt = min(8, t.ngroups - g0);
           if (!dwait(&s.empty[stage], phase ^ 1u, err)) {
@@ -852,17 +819,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the activation warp copies nr rows into the stage; a TMA box always
           // delivers its full size (out-of-range parts are zero-filled)
           mbar_arrive_expect_tx(&s.full[stage], kWB + (scale_tma ? kSB : 0) + t.nr * gcnt * 256);
-          uint8_t* st = stage_base + (size_t)stage * sb;
-          if (swz) {
-            tma_3d(smem_u32(st), tm, &s.full[stage], 0, g0 / 2, t.rowA0);
-            tma_3d(smem_u32(st + kWB / 2), tm, &s.full[stage], 0, g0 / 2, t.rowA1);
+          const uint32_t st = smem_u32(stage_base + (size_t)stage * sb);
+          if (!t.down) {
+            if (swz)
+              tma_4d(st, tm, &s.full[stage], 0, g0 / 2, t.tile * kTile1, half);
+            else
+              tma_3d(st, tm, &s.full[stage], g0 * 16, t.tile * kTile1, half);
+            if (scale_tma) tma_3d(st + kWB, ts, &s.full[stage], g0, t.tile * kTile1, half);
           } else {
-            tma_2d(smem_u32(st), tm, &s.full[stage], g0 * 16, t.rowA0);
-            tma_2d(smem_u32(st + kWB / 2), tm, &s.full[stage], g0 * 16, t.rowA1);
-          }
-          if (scale_tma) {
-            tma_2d(smem_u32(st + kWB), ts, &s.full[stage], g0, t.rowA0);
-            tma_2d(smem_u32(st + kWB + kSB / 2), ts, &s.full[stage], g0, t.rowA1);
+            if (swz)
+              tma_3d(st, tm, &s.full[stage], 0, g0 / 2, t.rowA0);
+            else
+              tma_2d(st, tm, &s.full[stage], g0 * 16, t.rowA0);
+            if (scale_tma) tma_2d(st + kWB, ts, &s.full[stage], g0, t.rowA0);
           }
           mbar_arrive(&s.desc_ready[stage]);
           if (++stage == nst) {
@@ -871,17 +840,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
-      stage = __shfl_sync(0xffffffffu, stage, 0);
-      phase = __shfl_sync(0xffffffffu, phase, 0);
+      if (!stop && dwait(&s.empty[stage], phase ^ 1u, err)) {
+        s.desc[stage].flags = kEnd;
+        mbar_arrive(&s.full[stage]);
+        mbar_arrive(&s.desc_ready[stage]);
+      }
     }
-    if (lane == 0 && !stop && dwait(&s.empty[stage], phase ^ 1u, err)) {
-      s.desc[stage].flags = kEnd;
-      mbar_arrive(&s.full[stage]);
-      mbar_arrive(&s.desc_ready[stage]);
-    }
+    __syncwarp();
   } else if (warp == kActs) {
     // ---------------------------------------------------------------- activation rows
+    // First this CTA's share of the tokens (t = b, b + G, ...): the
+    // interleaved copy of x that every CTA's gate/up stages read, published on
+    // its own counter. It needs no routing, so the shared expert's gate/up
+    // stages can complete while the router works.
+    {
+      const int h8 = d.H / 8;  // 16-byte chunks of a row; 16 per K group
+      for (int t = blockIdx.x; t < d.T; t += gridDim.x) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * d.H);
+        uint4* dst = reinterpret_cast<uint4*>(p.xi + (size_t)t * d.H);
+        for (int c0 = 0; c0 < h8; c0 += 32 * 8) {
+          uint4 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int cidx = c0 + u * 32 + lane;
+            if (cidx < h8) v[u] = __ldg(src + cidx);
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int cidx = c0 + u * 32 + lane;
+            if (cidx < h8) dst[(cidx & ~15) | chunk_t(cidx & 15)] = interleave8(v[u]);
+          }
+        }
+      }
+      __threadfence();
+      __syncwarp();
+      if (lane == 0 && (int)blockIdx.x < d.T) atomicAdd(&p.sync[1], 1u);
+    }
     int stage = 0;
     uint32_t phase = 0;
     bool routed_known = false, pre_ready = false;

@@ -43,12 +43,16 @@ struct moe_w4a16_handle {
   bool events_made = false;
   // tensor-map cache keyed by the tensor pointers it was encoded for:
   // 0 w13_q, 1 w2_q, 2 sh_w13_q, 3 sh_w2_q (3-D, 1-group boxes), 4 w13_s, 5 w2_s,
-  // 6 sh_w13_s, 7 sh_w2_s (scales), 8 w13_q, 9 w2_q, 10 sh_w13_q, 11 sh_w2_q
-  // (2-D, 8-group boxes), 12..15 the same weights in 128-row boxes
-  // (tensor-core experts)
+  // 6 sh_w13_s, 7 sh_w2_s (scales) of the GEMV engine, 12..15 the weights in
+  // 128-row boxes (tensor-core experts); 8..11 unused
   static constexpr int kMaps = 16;
   const void* map_keys[kMaps] = {};
   CUtensorMap maps[kMaps];
+  // tensor maps of the decode kernel, encoded for the weight pointers in
+  // dec_key (see encode_decode_maps)
+  moe_w4a16_weights dec_key{};
+  bool dec_ready = false;
+  DecodeWeights dec{};
   // views of the workspace's activation operands for the tensor-core experts
   CUtensorMap xmap, hmap;
   // tensor-core router: bf16 planes of router_w and the view of this call's x
@@ -207,40 +211,6 @@ int encode_scale_map(CUtensorMap* m, const void* base, long long rows, int K) {
   return MOE_W4A16_OK;
 }
 
-// Decode-kernel view of a packed INT4 tensor [rows, K/8] uint32: 8 K-groups
-// of 16 rows (8 KB) per box. When K is a multiple of 256 the rows are viewed
-// as 128-byte segments, {32 words, K/256 segments, rows}, box {32, 4, 16},
-// with the 128-byte swizzle (the consumers then read without bank
-// conflicts); otherwise a plain 2-D view {K/8 words, rows}, box {128, 16}.
-// The kernel picks its box form by the same rule.
-int encode_int4_map_decode(CUtensorMap* m, const void* base, long long rows, int K) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return MOE_W4A16_ERR_CUDA;
-  CUresult r;
-  if (K % 256 == 0) {
-    cuuint64_t dims[3] = {32, (cuuint64_t)(K / 256), (cuuint64_t)rows};
-    cuuint64_t strides[2] = {128, (cuuint64_t)K / 2};
-    cuuint32_t box[3] = {32, 4, 16};
-    cuuint32_t estr[3] = {1, 1, 1};
-    r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  } else {
-    cuuint64_t dims[2] = {(cuuint64_t)K / 8, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)K / 2};
-    cuuint32_t box[2] = {128, 16};
-    cuuint32_t estr[2] = {1, 1};
-    r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  }
-  if (r != CUDA_SUCCESS) {
-    fprintf(stderr, "moe_w4a16: cuTensorMapEncodeTiled (decode weights) failed (%d)\n", (int)r);
-    return MOE_W4A16_ERR_CUDA;
-  }
-  return MOE_W4A16_OK;
-}
-
 int encode_2d(CUtensorMap* m, CUtensorMapDataType type, int esize, const void* base,
               long long cols, long long rows, int box0, int box1, CUtensorMapSwizzle swz,
               CUtensorMapL2promotion l2, const char* what) {
@@ -255,6 +225,125 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType type, int esize, const void* b
   if (r != CUDA_SUCCESS) {
     fprintf(stderr, "moe_w4a16: cuTensorMapEncodeTiled (%s) failed (%d)\n", what, (int)r);
     return MOE_W4A16_ERR_CUDA;
+  }
+  return MOE_W4A16_OK;
+}
+
+int encode_nd(CUtensorMap* m, CUtensorMapDataType type, int rank, const void* base,
+              const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+              CUtensorMapSwizzle swz, CUtensorMapL2promotion l2, const char* what) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MOE_W4A16_ERR_CUDA;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, type, rank, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    fprintf(stderr, "moe_w4a16: cuTensorMapEncodeTiled (%s) failed (%d)\n", what, (int)r);
+    return MOE_W4A16_ERR_CUDA;
+  }
+  return MOE_W4A16_OK;
+}
+
+// Decode-kernel views: one box per stage brings both 16-row weight tiles of a
+// task (8 K-groups each), one more their group scales.
+//  gate/up, w13 [E', 2I', K/8] (K = H; E' = E, or 1 for the shared expert):
+//    K % 256 == 0: {32 words, K/256 segments, I' rows, 2E' halves}, box
+//                  {32, 4, 16, 2}, 128-byte swizzle
+//    otherwise:    {K/8 words, I' rows, 2E' halves}, box {128, 16, 2}
+//    scales [E', 2I', K/128]: {K/128, I', 2E'}, box {8, 16, 2}
+//  down, w2 [E'H rows, K/8] (K = I'):
+//    K % 256 == 0: {32 words, K/256 segments, rows}, box {32, 4, 32},
+//                  128-byte swizzle
+//    otherwise:    {K/8 words, rows}, box {128, 32}
+//    scales [rows, K/128]: {K/128, rows}, box {8, 32}
+// The scale views need K/128 to be a multiple of 8 (16-byte row stride); the
+// caller only encodes them then.
+int encode_decode_w13(CUtensorMap* m, const void* base, int halves, int inter, int K) {
+  if (K % 256 == 0) {
+    const cuuint64_t dims[4] = {32, (cuuint64_t)(K / 256), (cuuint64_t)inter, (cuuint64_t)halves};
+    const cuuint64_t str[3] = {128, (cuuint64_t)K / 2, (cuuint64_t)inter * (K / 2)};
+    const cuuint32_t box[4] = {32, 4, 16, 2};
+    return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, base, dims, str, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "decode w13");
+  }
+  const cuuint64_t dims[3] = {(cuuint64_t)(K / 8), (cuuint64_t)inter, (cuuint64_t)halves};
+  const cuuint64_t str[2] = {(cuuint64_t)K / 2, (cuuint64_t)inter * (K / 2)};
+  const cuuint32_t box[3] = {128, 16, 2};
+  return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, base, dims, str, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "decode w13");
+}
+int encode_decode_w2(CUtensorMap* m, const void* base, long long rows, int K) {
+  if (K % 256 == 0) {
+    const cuuint64_t dims[3] = {32, (cuuint64_t)(K / 256), (cuuint64_t)rows};
+    const cuuint64_t str[2] = {128, (cuuint64_t)K / 2};
+    const cuuint32_t box[3] = {32, 4, 32};
+    return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, base, dims, str, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "decode w2");
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)rows};
+  const cuuint64_t str[1] = {(cuuint64_t)K / 2};
+  const cuuint32_t box[2] = {128, 32};
+  return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, base, dims, str, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "decode w2");
+}
+int encode_decode_s13(CUtensorMap* m, const void* base, int halves, int inter, int K) {
+  const cuuint64_t dims[3] = {(cuuint64_t)(K / kGroup), (cuuint64_t)inter, (cuuint64_t)halves};
+  const cuuint64_t str[2] = {(cuuint64_t)(K / kGroup) * 2, (cuuint64_t)inter * (K / kGroup) * 2};
+  const cuuint32_t box[3] = {8, 16, 2};
+  return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, base, dims, str, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "decode w13 scales");
+}
+int encode_decode_s2(CUtensorMap* m, const void* base, long long rows, int K) {
+  const cuuint64_t dims[2] = {(cuuint64_t)(K / kGroup), (cuuint64_t)rows};
+  const cuuint64_t str[1] = {(cuuint64_t)(K / kGroup) * 2};
+  const cuuint32_t box[2] = {8, 32};
+  return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dims, str, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "decode w2 scales");
+}
+
+// Scales ride in the decode kernel's TMA stages when every K has a multiple
+// of 8 groups (16-byte rows of scales); otherwise the consumers read them.
+bool decode_scale_tma(const moe_w4a16_config& c) {
+  return (c.hidden / kGroup) % 8 == 0 && (c.inter / kGroup) % 8 == 0 &&
+         (c.shared_inter == 0 || (c.shared_inter / kGroup) % 8 == 0);
+}
+
+// Every input of the decode kernel that depends on the weights only.
+int encode_decode_maps(DecodeWeights* dw, const moe_w4a16_config& c, const moe_w4a16_weights* w) {
+  const bool has_sh = c.shared_inter > 0;
+  const bool scale_tma = decode_scale_tma(c);
+  const long long r2 = (long long)c.num_experts * c.hidden;
+  int st;
+  dw->router_w = w->router_w;
+  dw->router_bias = w->router_bias;
+  dw->s13_routed = w->w13_s;
+  dw->s13_shared = has_sh ? w->sh_w13_s : w->w13_s;
+  dw->s2_routed = w->w2_s;
+  dw->s2_shared = has_sh ? w->sh_w2_s : w->w2_s;
+  dw->scale_tma = scale_tma;
+  if ((st = encode_decode_w13(&dw->tm13r, w->w13_q, 2 * c.num_experts, c.inter, c.hidden)) != MOE_W4A16_OK ||
+      (st = encode_decode_w2(&dw->tm2r, w->w2_q, r2, c.inter)) != MOE_W4A16_OK)
+    return st;
+  dw->tm13s = dw->tm13r;
+  dw->tm2s = dw->tm2r;
+  if (has_sh && ((st = encode_decode_w13(&dw->tm13s, w->sh_w13_q, 2, c.shared_inter, c.hidden)) != MOE_W4A16_OK ||
+                 (st = encode_decode_w2(&dw->tm2s, w->sh_w2_q, c.hidden, c.shared_inter)) != MOE_W4A16_OK))
+    return st;
+  // without TMA-borne scales the scale maps are never used: copies of the
+  // weight maps keep the parameter block defined
+  dw->ts13r = dw->tm13r;
+  dw->ts2r = dw->tm2r;
+  dw->ts13s = dw->tm13s;
+  dw->ts2s = dw->tm2s;
+  if (scale_tma) {
+    if ((st = encode_decode_s13(&dw->ts13r, w->w13_s, 2 * c.num_experts, c.inter, c.hidden)) != MOE_W4A16_OK ||
+        (st = encode_decode_s2(&dw->ts2r, w->w2_s, r2, c.inter)) != MOE_W4A16_OK)
+      return st;
+    dw->ts13s = dw->ts13r;
+    dw->ts2s = dw->ts2r;
+    if (has_sh && ((st = encode_decode_s13(&dw->ts13s, w->sh_w13_s, 2, c.shared_inter, c.hidden)) != MOE_W4A16_OK ||
+                   (st = encode_decode_s2(&dw->ts2s, w->sh_w2_s, c.hidden, c.shared_inter)) != MOE_W4A16_OK))
+      return st;
   }
   return MOE_W4A16_OK;
 }
@@ -278,7 +367,6 @@ int get_map(moe_w4a16_handle* h, int slot, const void* base, long long rows, int
   if (h->map_keys[slot] == base && base) return MOE_W4A16_OK;
   const int st = slot < 4    ? encode_int4_map(&h->maps[slot], base, rows, K)
                  : slot < 8  ? encode_scale_map(&h->maps[slot], base, rows, K)
-                 : slot < 12 ? encode_int4_map_decode(&h->maps[slot], base, rows, K)
                              : encode_int4_map_tc(&h->maps[slot], base, rows, K);
   if (st == MOE_W4A16_OK) h->map_keys[slot] = base;
   return st;
@@ -489,10 +577,25 @@ int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t T, const m
   if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) cudaSetDevice(h->device);
 
   Dims d{T, c.hidden, c.num_experts, c.top_k, c.inter, c.shared_inter};
+  cudaError_t e;
+  if (T <= kSmallT && !(c.flags & MOE_W4A16_FLAG_FORCE_TC)) {
+    // decode sizes: the whole layer in one cooperative persistent kernel
+    if (!h->dec_ready || memcmp(&h->dec_key, w, sizeof(*w)) != 0) {
+      h->dec_ready = false;
+      if ((st = encode_decode_maps(&h->dec, c, w)) != MOE_W4A16_OK) return st;
+      h->dec_key = *w;
+      h->dec_ready = true;
+    }
+    const DecodeWeights& dw = h->dec;
+    if ((e = launch_decode(d, h->r, dw, x, h->r.xperm, h->h, h->hstride, h->y, out,
+                           h->counters, h->decode_grid, s, h->log)) != cudaSuccess)
+      return cuda_status(e);
+    h->last_T = T;
+    return MOE_W4A16_OK;
+  }
   const bool has_sh = c.shared_inter > 0;
   // scales ride in the TMA stages when every K has a multiple of 8 groups
-  const bool scale_tma = (c.hidden / kGroup) % 8 == 0 && (c.inter / kGroup) % 8 == 0 &&
-                         (!has_sh || (c.shared_inter / kGroup) % 8 == 0);
+  const bool scale_tma = decode_scale_tma(c);
   const long long r13 = (long long)c.num_experts * 2 * c.inter, r2 = (long long)c.num_experts * c.hidden;
   if ((st = get_map(h, 0, w->w13_q, r13, c.hidden)) != MOE_W4A16_OK) return st;
   if ((st = get_map(h, 1, w->w2_q, r2, c.inter)) != MOE_W4A16_OK) return st;
@@ -525,38 +628,6 @@ int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t T, const m
   g2.scale_shared = has_sh ? w->sh_w2_s : w->w2_s;
   g2.scale_tma = scale_tma;
 
-  cudaError_t e;
-  if (T <= kSmallT && !(c.flags & MOE_W4A16_FLAG_FORCE_TC)) {
-    // decode sizes: the whole layer in one cooperative persistent kernel
-    if ((st = get_map(h, 8, w->w13_q, r13, c.hidden)) != MOE_W4A16_OK) return st;
-    if ((st = get_map(h, 9, w->w2_q, r2, c.inter)) != MOE_W4A16_OK) return st;
-    if (has_sh) {
-      if ((st = get_map(h, 10, w->sh_w13_q, 2LL * c.shared_inter, c.hidden)) != MOE_W4A16_OK)
-        return st;
-      if ((st = get_map(h, 11, w->sh_w2_q, c.hidden, c.shared_inter)) != MOE_W4A16_OK) return st;
-    }
-    DecodeWeights dw;
-    dw.router_w = w->router_w;
-    dw.router_bias = w->router_bias;
-    dw.s13_routed = w->w13_s;
-    dw.s13_shared = has_sh ? w->sh_w13_s : w->w13_s;
-    dw.s2_routed = w->w2_s;
-    dw.s2_shared = has_sh ? w->sh_w2_s : w->w2_s;
-    dw.tm13r = h->maps[8];
-    dw.tm13s = has_sh ? h->maps[10] : h->maps[8];
-    dw.tm2r = h->maps[9];
-    dw.tm2s = has_sh ? h->maps[11] : h->maps[9];
-    dw.ts13r = g1.ts_routed;
-    dw.ts13s = g1.ts_shared;
-    dw.ts2r = g2.ts_routed;
-    dw.ts2s = g2.ts_shared;
-    dw.scale_tma = scale_tma;
-    if ((e = launch_decode(d, h->r, dw, x, h->r.xperm, h->h, h->hstride, h->y, out,
-                           h->counters, h->decode_grid, s, h->log)) != cudaSuccess)
-      return cuda_status(e);
-    h->last_T = T;
-    return MOE_W4A16_OK;
-  }
   const bool use_tc = h->tc_ok && !(c.flags & MOE_W4A16_FLAG_FORCE_GEMV);
   if (use_tc) {
     // tensor-core experts: routing also gathers x into expert order
@@ -871,42 +942,8 @@ extern "C" int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint
   const int hstride = c.inter > c.shared_inter ? c.inter : c.shared_inter;
 
   // tensor maps, encoded on the host for this call
-  const bool has_sh = c.shared_inter > 0;
-  const bool scale_tma = (c.hidden / kGroup) % 8 == 0 && (c.inter / kGroup) % 8 == 0 &&
-                         (!has_sh || (c.shared_inter / kGroup) % 8 == 0);
-  const long long r13 = (long long)c.num_experts * 2 * c.inter, r2 = (long long)c.num_experts * c.hidden;
   DecodeWeights dw;
-  dw.router_w = w->router_w;
-  dw.router_bias = w->router_bias;
-  dw.s13_routed = w->w13_s;
-  dw.s13_shared = has_sh ? w->sh_w13_s : w->w13_s;
-  dw.s2_routed = w->w2_s;
-  dw.s2_shared = has_sh ? w->sh_w2_s : w->w2_s;
-  dw.scale_tma = scale_tma;
-  if ((st = encode_int4_map_decode(&dw.tm13r, w->w13_q, r13, c.hidden)) != MOE_W4A16_OK) return st;
-  if ((st = encode_int4_map_decode(&dw.tm2r, w->w2_q, r2, c.inter)) != MOE_W4A16_OK) return st;
-  dw.tm13s = dw.tm13r;
-  dw.tm2s = dw.tm2r;
-  if (has_sh) {
-    if ((st = encode_int4_map_decode(&dw.tm13s, w->sh_w13_q, 2LL * c.shared_inter, c.hidden)) != MOE_W4A16_OK)
-      return st;
-    if ((st = encode_int4_map_decode(&dw.tm2s, w->sh_w2_q, c.hidden, c.shared_inter)) != MOE_W4A16_OK)
-      return st;
-  }
-  dw.ts13r = dw.tm13r;
-  dw.ts2r = dw.tm2r;
-  if (scale_tma) {
-    if ((st = encode_scale_map(&dw.ts13r, w->w13_s, r13, c.hidden)) != MOE_W4A16_OK) return st;
-    if ((st = encode_scale_map(&dw.ts2r, w->w2_s, r2, c.inter)) != MOE_W4A16_OK) return st;
-  }
-  dw.ts13s = dw.ts13r;
-  dw.ts2s = dw.ts2r;
-  if (scale_tma && has_sh) {
-    if ((st = encode_scale_map(&dw.ts13s, w->sh_w13_s, 2LL * c.shared_inter, c.hidden)) != MOE_W4A16_OK)
-      return st;
-    if ((st = encode_scale_map(&dw.ts2s, w->sh_w2_s, c.hidden, c.shared_inter)) != MOE_W4A16_OK)
-      return st;
-  }
+  if ((st = encode_decode_maps(&dw, c, w)) != MOE_W4A16_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: clear the counters and
