@@ -304,3 +304,22 @@ def test_prefill8192_outputs_cover_every_active_expert(full):
     assert (np.diff(rt["offsets"]) > 0).all()
     assert names[-3:] == ["tc_gate_up_swiglu", "tc_down", "combine"]
     assert subset.size >= 256
+
+
+def test_zipf2048_repeated_forwards_are_bit_identical(full):
+    # Zipf routing puts ~90 experts with under 10 rows on the tensor-core path
+    # next to a 2048-row expert: tiny and full N-tiles in the same persistent
+    # schedule. Every forward of the same input must give the same bits.
+    shape = ms.CONFIGS["zipf2048"]
+    layer = mc.layer_with_tokens(shape)
+    obj = _layer_obj(layer, full, shape.tokens, bias=layer.router_b)
+    x = upload_tokens(layer.x, DEV)
+    first = obj.forward(x)
+    torch.cuda.synchronize()
+    first = first.cpu().numpy()
+    for _ in range(40):
+        again = obj.forward(x)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(again.cpu().numpy(), first)
+    assert moe.moe_w4a16_check_device_errors(obj.handle) == 0
+    obj.close()
