@@ -26,21 +26,26 @@
 //    keeps the critical path at two global round trips, and it overlaps the
 //    shared expert's work, which needs no routing.
 //  * 8 consumer warps stream stages from the start: warp w takes K-group w of
-//    both tiles (the activation fragments serve both; one MMA chain per
-//    tile); exact INT4 -> bf16 in registers (lop3 into the mantissa, a bf16x2
-//    subtract), mma.sync m16n8k16 with the weights as A and up to 8 rows as
-//    B, group scales applied in fp32. At the end of a task each warp drops its
-//    partial sums into a slot and moves on. Every stage reads its activation
-//    rows (the interleaved x that the CTAs owning a token prepare once per
-//    forward, or h) in one layout, so all stages share one code path.
-//  * 1 weight producer warp: decodes tasks and fills a ring of stages (TMA
-//    boxes of 16 rows x 512 B per tile, 128-byte swizzled when K is a
-//    multiple of 256, and scale boxes) with a descriptor per
+//    both tiles in each 8-group sub-stage (the activation fragments serve
+//    both; one MMA chain per tile); exact INT4 -> bf16 in registers (lop3
+//    into the mantissa, a bf16x2 subtract), mma.sync m16n8k16 with the
+//    weights as A and up to 8 rows as B, group scales applied in fp32. At the
+//    end of a task each warp drops its partial sums into a slot and moves on.
+//    Every stage reads its activation rows (the interleaved x that the CTAs
+//    owning a token prepare once per forward, or h) in one layout, so all
+//    stages share one code path.
+//  * 1 weight producer warp: fills a ring of stages with a descriptor per
 //    stage; it only ever waits for free stages, so the weight stream never
-//    stops on a dependency. A stage holds the weights plus room for the
-//    pass's activation rows (min(T, 8)), so a small batch gets more stages:
-//    at one token 9 stages (144 KB of weights in flight per SM) instead of 5
-//    at 64 tokens, enough to cover the ~1.5 us a weight box takes to arrive.
+//    stops on a dependency. The shared expert's gate/up tasks it decodes
+//    itself; from the first routed task on it reads records that the router
+//    warps decoded next to the routing. A stage holds the weights plus room
+//    for the pass's activation rows (min(T, 8)). Up to 4 rows, and when every
+//    K is a multiple of 1024, a stage is 16 K-groups (32 KB of weights in one
+//    TMA box, its scales in another): 4 stages at one token (128 KB in flight
+//    per SM). Otherwise a stage is 8 K-groups (16 rows x 512 B per tile,
+//    128-byte swizzled when K is a multiple of 256): 5 stages at 64 tokens.
+//    Every handoff (descriptor, barrier waits and arrivals, TMA issues) is
+//    per stage, so the wide stage halves them per byte.
 //  * 1 activation warp: in ring order, copies each stage's activation rows
 //    (interleaved x for gate/up, h for down) into the stage (1-D bulk copies). Down tasks
 //    need the h rows of their (expert, pass): it polls the completion counters
@@ -76,22 +81,24 @@ constexpr int kThreads = (kCW + 2 + kEW + kRW) * 32;
 constexpr int kSW = kRW + kEW;               // warps that score experts (router + epilogue)
 constexpr int kR = 8;                        // rows per pass (MMA N)
 constexpr int kMaxS = 12;                    // ring stages at most (the count depends on T)
-constexpr int kWB = 2 * 16 * 512;            // 2 tiles x 16 rows x 512 B (8 K-groups)
-constexpr int kSB = 2 * 16 * 16;             // 2 tiles x 16 rows x 8 bf16 scales
-constexpr int kXS = 8 * 256 + 64;            // one activation row (8 groups bf16) + pad
-constexpr int kXO = kWB + kSB;
+constexpr int kWB = 2 * 16 * 512;            // sub-stage: 2 tiles x 16 rows x 512 B (8 K-groups)
+constexpr int kSB = 2 * 16 * 16;             // sub-stage: 2 tiles x 16 rows x 8 bf16 scales
+constexpr int kXSub = 8 * 256;               // one activation row of a sub-stage (8 groups bf16)
+constexpr int kMaxSub = 2;                   // sub-stages per stage at most
+constexpr int kWideRows = 4;                 // batches of at most this many tokens use 2 sub-stages
 constexpr int kSmemMax = 227 * 1024;         // opt-in shared memory of one CTA
 constexpr int kMaxPass = (kSmallT + kR - 1) / kR;  // passes per expert at most
 constexpr int kPairs = (kMaxExperts + 1) * kMaxPass;  // (expert, pass) counters
 constexpr int kItems = kSmallT * kMaxTopK;
+constexpr int kMaxRecs = 512;                // a CTA's tasks after routing, kept as decoded records
 
 // Stage descriptor flags. The consumers read only this word of a stage's
-// descriptor: the K groups of the stage sit in bits 8-11 and the activation
-// rows in bits 12-15.
+// descriptor: the K groups of the stage sit in bits 8-12 and the activation
+// rows in bits 13-16.
 // kPre: a gate/up stage, whose activation rows are the interleaved x.
 enum { kFirst = 1, kLast = 2, kEnd = 4, kShared = 8, kDown = 16, kPre = 32, kSwz = 64 };
 __host__ __device__ constexpr int stage_key(int flags, int gcnt, int nr) {
-  return flags | (gcnt << 8) | (nr << 12);
+  return flags | (gcnt << 8) | (nr << 13);
 }
 
 struct Desc {
@@ -116,6 +123,8 @@ struct Smem {
   int offsets[kMaxExperts + 2];
   int4 scan[kRW];
   int meta[4];                          // n_act, routed gate/up tasks, routed down tasks
+  uint2 trec[kMaxRecs];                 // this CTA's tasks from its first routed one on (task_record)
+  int nrec;                             // records in trec, or -1 (too many: decode on the fly)
   uint64_t full[kMaxS];
   uint64_t empty[kMaxS];
   uint64_t desc_ready[kMaxS];           // weight producer -> activation warp
@@ -152,6 +161,8 @@ struct DecodeParams {
   int scale_tma;
   int nst;                      // ring stages
   int stage_bytes;              // bytes per stage (a multiple of 1024)
+  int nsub;                     // sub-stages (8 K-groups each) per stage
+  int xs;                       // bytes per activation row of a stage (nsub groups of 8, + pad)
 };
 
 struct Task {
@@ -247,6 +258,16 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, uin
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_5d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
+                                       int c0, int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(c4)
       : "memory");
 }
 
@@ -372,6 +393,38 @@ __device__ __forceinline__ Task task_at(const Smem& s, const Dims& d, const Coun
   }
   Task t{};
   t.ngroups = 0;
+  return t;
+}
+
+// A task in two words: expert (9 bits), tile (12), pass (3), down, shared;
+// first row (16), rows (16).
+__device__ __forceinline__ uint2 task_record(const Task& t) {
+  return make_uint2((uint32_t)t.e | ((uint32_t)t.tile << 9) | ((uint32_t)t.pass << 21) |
+                        ((uint32_t)t.down << 24) | ((uint32_t)t.shared << 25),
+                    (uint32_t)t.r0 | ((uint32_t)t.nr << 16));
+}
+
+__device__ __forceinline__ Task task_of_record(const Dims& d, uint2 r) {
+  Task t;
+  t.e = (int)(r.x & 511u);
+  t.tile = (int)((r.x >> 9) & 4095u);
+  t.pass = (int)((r.x >> 21) & 7u);
+  t.down = ((r.x >> 24) & 1u) != 0;
+  t.shared = ((r.x >> 25) & 1u) != 0;
+  t.r0 = (int)(r.y & 0xffffu);
+  t.nr = (int)(r.y >> 16);
+  const int inter = t.shared ? d.Is : d.I;
+  if (!t.down) {
+    t.ngroups = d.H / kGroup;
+    t.rowA0 = (t.shared ? 0 : t.e * 2 * inter) + t.tile * kTile1;
+    t.rowA1 = t.rowA0 + inter;
+    t.cnt_target = 0;
+  } else {
+    t.ngroups = inter / kGroup;
+    t.rowA0 = (t.shared ? 0 : t.e * d.H) + t.tile * kTile2;
+    t.rowA1 = t.rowA0 + 16;
+    t.cnt_target = inter / kTile1;
+  }
   return t;
 }
 
@@ -675,6 +728,25 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
   }
   rbar();
   const int n = d.T * d.k;
+  if (warp > 0) {
+    // this CTA's tasks from its first routed one on (tau = first, first + G,
+    // ...), decoded into records by the other router warps while warp 0
+    // builds the permutation; the weight producer reads one record per task
+    Counts c;
+    c.sh1 = d.Is > 0 ? (d.Is / kTile1) * passes_of(d.T) : 0;
+    c.sh2 = d.Is > 0 ? (d.H / kTile2) * passes_of(d.T) : 0;
+    c.n_act = s.meta[0];
+    c.r1 = s.meta[1];
+    c.r2 = s.meta[2];
+    const int b = blockIdx.x, G = gridDim.x;
+    const int total = c.sh1 + c.r1 + c.sh2 + c.r2;
+    const int first = c.sh1 <= b ? b : b + ((c.sh1 - b + G - 1) / G) * G;
+    const int nrec = first < total ? (total - first + G - 1) / G : 0;
+    if (tid == 32) s.nrec = nrec <= kMaxRecs ? nrec : -1;
+    if (nrec <= kMaxRecs)
+      for (int j = tid - 32; j < nrec; j += (kRW - 1) * 32)
+        s.trec[j] = task_record(task_at(s, d, c, first + j * G));
+  }
   if (warp == 0) {
     // stable placement, 32 items at a time: rank among equal experts in the
     // chunk by __match_any_sync, plus the expert's running count
@@ -781,29 +853,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool known = false, stop = false;
       int stage = 0;
       uint32_t phase = 0;
+      const int nsub = p.nsub, gps = 8 * nsub;  // K groups per stage
+      int rec = 0, nrec = -1;
       for (int tau = blockIdx.x; !stop; tau += gridDim.x) {
         if (tau >= cnt.sh1 && !known) {
           if (!dwait(&s.route_ready, 0, err)) break;
           cnt.n_act = s.meta[0];
           cnt.r1 = s.meta[1];
           cnt.r2 = s.meta[2];
+          nrec = s.nrec;
           known = true;
         }
-        const Task t = task_at(s, d, cnt, tau);
+        Task t;
+        if (known && nrec >= 0) {
+          if (rec >= nrec) break;  // past the last task
+          t = task_of_record(d, s.trec[rec++]);
+        } else {
+          t = task_at(s, d, cnt, tau);
+        }
         if (t.ngroups == 0) break;  // past the last task
         const CUtensorMap* tm = t.down ? (t.shared ? &tm2s : &tm2r) : (t.shared ? &tm13s : &tm13r);
         const CUtensorMap* ts = t.down ? (t.shared ? &ts2s : &ts2r) : (t.shared ? &ts13s : &ts13r);
         const bool swz = swizzled_k(t.ngroups * kGroup);
         const int half = t.shared ? 0 : 2 * t.e;  // gate half of the expert (up: half + 1)
-        for (int g0 = 0; g0 < t.ngroups; g0 += 8) {
-          const int gcnt = min(8, t.ngroups - g0);
+        for (int g0 = 0; g0 < t.ngroups; g0 += gps) {
+          const int gcnt = min(gps, t.ngroups - g0);
           if (!dwait(&s.empty[stage], phase ^ 1u, err)) {
             stop = true;
             break;
           }
           Desc& ds = s.desc[stage];
           const bool pre = !t.down;  // gate/up: the interleaved x rows
-          ds.flags = stage_key((g0 == 0 ? kFirst : 0) | (g0 + 8 >= t.ngroups ? kLast : 0) |
+          ds.flags = stage_key((g0 == 0 ? kFirst : 0) | (g0 + gps >= t.ngroups ? kLast : 0) |
                                    (t.shared ? kShared : 0) | (t.down ? kDown : 0) |
                                    (pre ? kPre : 0) | (swz ? kSwz : 0),
                                gcnt, t.nr);
@@ -818,20 +899,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           ds.cnt = t.e * kMaxPass + t.pass;
           // the activation warp copies nr rows into the stage; a TMA box always
           // delivers its full size (out-of-range parts are zero-filled)
-          mbar_arrive_expect_tx(&s.full[stage], kWB + (scale_tma ? kSB : 0) + t.nr * gcnt * 256);
-          const uint32_t st = smem_u32(stage_base + (size_t)stage * sb);
-          if (!t.down) {
+          // a box always delivers its full size (out-of-range parts are
+          // zero-filled); the activation warp copies nr rows into the stage
+          mbar_arrive_expect_tx(&s.full[stage], nsub * (kWB + (scale_tma ? kSB : 0)) + t.nr * gcnt * 256);
+          const uint32_t st = smem_u32(stage_base + (size_t)stage * sb), ss = st + nsub * kWB;
+          if (nsub == 2) {
+            // wide views: 16 K groups of both tiles in one box
+            if (!t.down) {
+              tma_5d(st, tm, &s.full[stage], 0, 0, t.tile * kTile1, g0 / 8, half);
+              if (scale_tma) tma_3d(ss, ts, &s.full[stage], g0, t.tile * kTile1, half);
+            } else {
+              tma_5d(st, tm, &s.full[stage], 0, 0, 0, g0 / 8, t.rowA0 / 16);
+              if (scale_tma) tma_2d(ss, ts, &s.full[stage], g0, t.rowA0);
+            }
+          } else if (!t.down) {
             if (swz)
               tma_4d(st, tm, &s.full[stage], 0, g0 / 2, t.tile * kTile1, half);
             else
               tma_3d(st, tm, &s.full[stage], g0 * 16, t.tile * kTile1, half);
-            if (scale_tma) tma_3d(st + kWB, ts, &s.full[stage], g0, t.tile * kTile1, half);
+            if (scale_tma) tma_3d(ss, ts, &s.full[stage], g0, t.tile * kTile1, half);
           } else {
             if (swz)
               tma_3d(st, tm, &s.full[stage], 0, g0 / 2, t.rowA0);
             else
               tma_2d(st, tm, &s.full[stage], g0 * 16, t.rowA0);
-            if (scale_tma) tma_2d(st + kWB, ts, &s.full[stage], g0, t.rowA0);
+            if (scale_tma) tma_2d(ss, ts, &s.full[stage], g0, t.rowA0);
           }
           mbar_arrive(&s.desc_ready[stage]);
           if (++stage == nst) {
@@ -943,7 +1035,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (lane < ds.nr) {
         const int r = ds.r0 + lane;
-        const uint32_t slot = smem_u32(stage_base + (size_t)stage * sb + kXO + lane * kXS);
+        const uint32_t slot =
+            smem_u32(stage_base + (size_t)stage * sb + p.nsub * (kWB + kSB) + lane * p.xs);
         const uint16_t* src;
         if (!down) {
           const int tok = (ds.flags & kShared) ? r - d.T * d.k : s.perm_s[r];
@@ -968,8 +1061,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t seg = (uint32_t)gw >> 1;
     const uint32_t w_off_s =
         g * 512 + seg * 128 + (((((uint32_t)(gw & 1) << 2) | c) ^ (seg | ((uint32_t)(g & 1) << 2))) << 4);
-    const uint32_t s_off = kWB + g * 16 + gw * 2;
-    const uint32_t xt_off = kXO + g * kXS + gw * 256 + c * 16;  // transposed (xi, h)
+    // a stage is [tile][sub-stage][16 rows][512 B] of weights, then the
+    // scales [tile][16 rows][8 nsub], then the activation rows
+    const int nsub = p.nsub;
+    const uint32_t tstride = nsub * (kWB / 2), sstride = nsub * (kSB / 2);  // per tile
+    const uint32_t s_off = nsub * kWB + g * 16 * nsub + gw * 2;
+    const uint32_t xt_off = nsub * (kWB + kSB) + g * p.xs + gw * 256 + c * 16;  // transposed (xi, h)
     int stage = 0;
     uint32_t phase = 0;
     int tseq = 0;  // tasks finished (the same sequence for all consumer warps)
@@ -982,26 +1079,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[0][i] = acc[1][i] = 0.f;
       }
-      const int gcnt = (key >> 8) & 15, nr = (key >> 12) & 15;
-      if (gw < gcnt) {
-        const uint32_t st = stage0 + stage * sb;
+      const int gcnt = (key >> 8) & 31, nr = (key >> 13) & 15;
+      // sub-stage j: K groups 8 j .. 8 j + 7 of the stage; this warp takes group 8 j + gw
+#pragma unroll
+      for (int j = 0; j < kMaxSub; ++j) {
+        if (j >= nsub || 8 * j + gw >= gcnt) break;
+        const uint32_t st = stage0 + stage * sb + j * (kWB / 2);  // + tile: this sub-stage's weights
+        const uint32_t sj = stage0 + stage * sb + j * 16;  // + s_off: its scales
+        const uint32_t xj = stage0 + stage * sb + j * kXSub;  // + xt_off: its activations
         const uint32_t wo = (key & kSwz) ? w_off_s : w_off;
         uint4 wA[2], wB[2];
         float sc[2][2];  // [tile][row g / g + 8]
 #pragma unroll
         for (int tl = 0; tl < 2; ++tl) {
-          wA[tl] = lds128(st + tl * (kWB / 2) + wo);
-          wB[tl] = lds128(st + tl * (kWB / 2) + wo + 8 * 512);
+          wA[tl] = lds128(st + tl * tstride + wo);
+          wB[tl] = lds128(st + tl * tstride + wo + 8 * 512);
           if (scale_tma) {
-            sc[tl][0] = bf16_bits_to_f32(lds16(st + tl * (kSB / 2) + s_off));
-            sc[tl][1] = bf16_bits_to_f32(lds16(st + tl * (kSB / 2) + s_off + 8 * 16));
+            sc[tl][0] = bf16_bits_to_f32(lds16(sj + tl * sstride + s_off));
+            sc[tl][1] = bf16_bits_to_f32(lds16(sj + tl * sstride + s_off + 8 * 16 * nsub));
           } else {
             const Desc& dd = s.desc[stage];
             const uint16_t* scl = (key & kDown) ? ((key & kShared) ? p.s2_shared : p.s2_routed)
                                                 : ((key & kShared) ? p.s13_shared : p.s13_routed);
             const int row = (tl ? dd.rowA1 : dd.rowA0) + g;
-            sc[tl][0] = bf16_bits_to_f32(__ldg(scl + (size_t)row * dd.ngroups + dd.g0 + gw));
-            sc[tl][1] = bf16_bits_to_f32(__ldg(scl + (size_t)(row + 8) * dd.ngroups + dd.g0 + gw));
+            const int grp = dd.g0 + 8 * j + gw;
+            sc[tl][0] = bf16_bits_to_f32(__ldg(scl + (size_t)row * dd.ngroups + grp));
+            sc[tl][1] = bf16_bits_to_f32(__ldg(scl + (size_t)(row + 8) * dd.ngroups + grp));
           }
         }
         // activation rows (interleaved x, or h) store chunk 4c + m of a K
@@ -1010,7 +1113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint4 b[4];
         if (g < nr) {
 #pragma unroll
-          for (int m = 0; m < 4; ++m) b[m] = lds128(st + xt_off + m * 64);
+          for (int m = 0; m < 4; ++m) b[m] = lds128(xj + xt_off + m * 64);
         } else {
 #pragma unroll
           for (int m = 0; m < 4; ++m) b[m] = make_uint4(0u, 0u, 0u, 0u);
@@ -1173,10 +1276,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 // Ring geometry for a batch of T tokens: as many stages as fit (at most
-// kMaxS), each holding min(T, kR) activation rows.
-static void ring_of(int T, int* nst, int* stage_bytes) {
+// kMaxS), each holding min(T, kR) activation rows. Up to kWideRows rows a
+// stage holds two sub-stages (16 K groups): half the per-stage hand-offs of
+// every warp role for the same bytes in flight.
+static void ring_of(int T, bool wide, int* nst, int* stage_bytes, int* nsub, int* xs) {
   const int rows = T < kR ? (T < 1 ? 1 : T) : kR;
-  *stage_bytes = (kXO + rows * kXS + 1023) / 1024 * 1024;
+  *nsub = wide && rows <= kWideRows ? kMaxSub : 1;
+  *xs = *nsub * kXSub + 64;  // rows 64 bytes off a multiple of 128: conflict-free reads
+  *stage_bytes = (*nsub * (kWB + kSB) + rows * *xs + 1023) / 1024 * 1024;
   const int n = (kSmemMax - kStageOff) / *stage_bytes;
   *nst = n < kMaxS ? n : kMaxS;
 }
@@ -1185,8 +1292,8 @@ cudaError_t decode_setup(int* ctas_per_sm) {
   cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemMax);
   if (e != cudaSuccess) return e;
-  int nst, sb;
-  ring_of(kSmallT, &nst, &sb);
+  int nst, sb, nsub, xs;
+  ring_of(kSmallT, false, &nst, &sb, &nsub, &xs);
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_kernel, kThreads,
                                                        kStageOff + nst * sb);
 }
@@ -1215,7 +1322,7 @@ cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& 
   p.tile_cnt = counters + (size_t)(d.E + 1) * kMaxPass;
   p.sync = reinterpret_cast<unsigned*>(p.tile_cnt + d.H / kTile2);
   p.scale_tma = w.scale_tma;
-  ring_of(d.T, &p.nst, &p.stage_bytes);
+  ring_of(d.T, w.wide != 0, &p.nst, &p.stage_bytes, &p.nsub, &p.xs);
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -1228,8 +1335,11 @@ cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   log.begin("decode_fused", s);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel, w.tm13r, w.tm13s, w.tm2r, w.tm2s,
-                                     w.ts13r, w.ts13s, w.ts2r, w.ts2s, p);
+  cudaError_t e =
+      p.nsub == 2 ? cudaLaunchKernelEx(&cfg, decode_kernel, w.wtm13r, w.wtm13s, w.wtm2r, w.wtm2s,
+                                       w.wts13r, w.wts13s, w.wts2r, w.wts2s, p)
+                  : cudaLaunchKernelEx(&cfg, decode_kernel, w.tm13r, w.tm13s, w.tm2r, w.tm2s,
+                                       w.ts13r, w.ts13s, w.ts2r, w.ts2s, p);
   log.end(s);
   return e;
 }

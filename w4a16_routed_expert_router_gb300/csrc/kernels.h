@@ -81,6 +81,10 @@ struct DecodeWeights {
   // 2-D views of the scales {K/128, rows}, box {8, 16} (when scale_tma)
   CUtensorMap ts13r, ts13s, ts2r, ts2s;
   int scale_tma;
+  // wide views (when every K is a multiple of 1024): one box brings 16
+  // K-groups of both 16-row tiles, one more their scales
+  CUtensorMap wtm13r, wtm13s, wtm2r, wtm2s, wts13r, wts13s, wts2r, wts2s;
+  int wide;
 };
 cudaError_t decode_setup(int* ctas_per_sm);
 size_t decode_counter_ints(int E, int H);

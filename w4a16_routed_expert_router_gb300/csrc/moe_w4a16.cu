@@ -238,7 +238,7 @@ int encode_nd(CUtensorMap* m, CUtensorMapDataType type, int rank, const void* ba
   CUresult r = fn(m, type, rank, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
-    fprintf(stderr, "moe_w4a16: cuTensorMapEncodeTiled (%s) failed (%d)\n", what, (int)r);
+    if (what) fprintf(stderr, "moe_w4a16: cuTensorMapEncodeTiled (%s) failed (%d)\n", what, (int)r);
     return MOE_W4A16_ERR_CUDA;
   }
   return MOE_W4A16_OK;
@@ -301,6 +301,44 @@ int encode_decode_s2(CUtensorMap* m, const void* base, long long rows, int K) {
                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, "decode w2 scales");
 }
 
+// Wide decode views (every K a multiple of 1024): a stage of 16 K-groups in
+// one box, laid out as [tile][half of the 16 groups][16 rows][512 B], each
+// 8 KB block with the 128-byte swizzle of the narrow views. The group-half
+// dimension (stride 512 B) sits between the rows and the tiles, so the rows
+// of a block stay 512 bytes apart.
+//  gate/up: {32 words, 4 segments, I' rows, K/1024, 2E' halves}, box {32, 4, 16, 2, 2}
+//  down:    {32 words, 4 segments, 16 rows, K/1024, E'H/16 tiles}, box {32, 4, 16, 2, 2}
+//  scales:  {K/128, I', 2E'} box {16, 16, 2}; {K/128, rows} box {16, 32}
+// An encode the driver refuses leaves the caller on the narrow views.
+int encode_decode_w13_wide(CUtensorMap* m, const void* base, int halves, int inter, int K) {
+  const cuuint64_t dims[5] = {32, 4, (cuuint64_t)inter, (cuuint64_t)(K / 1024), (cuuint64_t)halves};
+  const cuuint64_t str[4] = {128, (cuuint64_t)K / 2, 512, (cuuint64_t)inter * (K / 2)};
+  const cuuint32_t box[5] = {32, 4, 16, 2, 2};
+  return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 5, base, dims, str, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, nullptr);
+}
+int encode_decode_w2_wide(CUtensorMap* m, const void* base, long long rows, int K) {
+  const cuuint64_t dims[5] = {32, 4, 16, (cuuint64_t)(K / 1024), (cuuint64_t)(rows / 16)};
+  const cuuint64_t str[4] = {128, (cuuint64_t)K / 2, 512, (cuuint64_t)16 * (K / 2)};
+  const cuuint32_t box[5] = {32, 4, 16, 2, 2};
+  return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 5, base, dims, str, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, nullptr);
+}
+int encode_decode_s13_wide(CUtensorMap* m, const void* base, int halves, int inter, int K) {
+  const cuuint64_t dims[3] = {(cuuint64_t)(K / kGroup), (cuuint64_t)inter, (cuuint64_t)halves};
+  const cuuint64_t str[2] = {(cuuint64_t)(K / kGroup) * 2, (cuuint64_t)inter * (K / kGroup) * 2};
+  const cuuint32_t box[3] = {16, 16, 2};
+  return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, base, dims, str, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, nullptr);
+}
+int encode_decode_s2_wide(CUtensorMap* m, const void* base, long long rows, int K) {
+  const cuuint64_t dims[2] = {(cuuint64_t)(K / kGroup), (cuuint64_t)rows};
+  const cuuint64_t str[1] = {(cuuint64_t)(K / kGroup) * 2};
+  const cuuint32_t box[2] = {16, 32};
+  return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dims, str, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, nullptr);
+}
+
 // Scales ride in the decode kernel's TMA stages when every K has a multiple
 // of 8 groups (16-byte rows of scales); otherwise the consumers read them.
 bool decode_scale_tma(const moe_w4a16_config& c) {
@@ -344,6 +382,33 @@ int encode_decode_maps(DecodeWeights* dw, const moe_w4a16_config& c, const moe_w
     if (has_sh && ((st = encode_decode_s13(&dw->ts13s, w->sh_w13_s, 2, c.shared_inter, c.hidden)) != MOE_W4A16_OK ||
                    (st = encode_decode_s2(&dw->ts2s, w->sh_w2_s, c.hidden, c.shared_inter)) != MOE_W4A16_OK))
       return st;
+  }
+  // the wide views, when every K allows them (else, or when the driver
+  // refuses one, the kernel keeps to the narrow ones)
+  dw->wide = 0;
+  const bool wide_k = c.hidden % 1024 == 0 && c.inter % 1024 == 0 && (!has_sh || c.shared_inter % 1024 == 0);
+  if (wide_k) {
+    bool ok = encode_decode_w13_wide(&dw->wtm13r, w->w13_q, 2 * c.num_experts, c.inter, c.hidden) == MOE_W4A16_OK &&
+              encode_decode_w2_wide(&dw->wtm2r, w->w2_q, r2, c.inter) == MOE_W4A16_OK;
+    dw->wtm13s = dw->wtm13r;
+    dw->wtm2s = dw->wtm2r;
+    if (ok && has_sh)
+      ok = encode_decode_w13_wide(&dw->wtm13s, w->sh_w13_q, 2, c.shared_inter, c.hidden) == MOE_W4A16_OK &&
+           encode_decode_w2_wide(&dw->wtm2s, w->sh_w2_q, c.hidden, c.shared_inter) == MOE_W4A16_OK;
+    dw->wts13r = dw->wtm13r;
+    dw->wts2r = dw->wtm2r;
+    dw->wts13s = dw->wtm13s;
+    dw->wts2s = dw->wtm2s;
+    if (ok && scale_tma) {
+      ok = encode_decode_s13_wide(&dw->wts13r, w->w13_s, 2 * c.num_experts, c.inter, c.hidden) == MOE_W4A16_OK &&
+           encode_decode_s2_wide(&dw->wts2r, w->w2_s, r2, c.inter) == MOE_W4A16_OK;
+      dw->wts13s = dw->wts13r;
+      dw->wts2s = dw->wts2r;
+      if (ok && has_sh)
+        ok = encode_decode_s13_wide(&dw->wts13s, w->sh_w13_s, 2, c.shared_inter, c.hidden) == MOE_W4A16_OK &&
+             encode_decode_s2_wide(&dw->wts2s, w->sh_w2_s, c.hidden, c.shared_inter) == MOE_W4A16_OK;
+    }
+    dw->wide = ok ? 1 : 0;
   }
   return MOE_W4A16_OK;
 }
