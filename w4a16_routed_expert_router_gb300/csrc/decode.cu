@@ -131,7 +131,9 @@ struct Smem {
   unsigned pair_done[(kPairs + 31) / 32];  // finished (expert, pass) gate/up work
   uint64_t slot_full[kEW];
   uint64_t slot_free[kEW];
-  uint64_t route_ready;
+  uint64_t route_ready;                 // routing in shared memory (router warp 0)
+  uint64_t rec_ready;                   // task records (router warps 1-3)
+  uint64_t scored;                      // this CTA's logits published
   int flag;
 };
 
@@ -451,7 +453,7 @@ __device__ __forceinline__ void warp_topk(const float (&lg)[kPer], const float* 
   for (int i = 0; i < kPer; ++i) {
     const int e = lane + 32 * i;
     if (e < E) {
-      sc[i] = 1.0f / (1.0f + expf(-lg[i]));
+      sc[i] = __frcp_rn(1.0f + expf(-lg[i]));  // = 1 / (1 + e^-l), correctly rounded
       key[i] = fkey(sc[i] + bias[e]);
     } else {
       sc[i] = 0.f;
@@ -553,6 +555,8 @@ __device__ __forceinline__ int4 rscan4(int4 v, int t, int4* scr, int4* total) {
 __device__ __forceinline__ int scoring_warps(const Dims& d) { return d.T <= 4 ? kSW : kRW; }
 
 // named barrier of the scoring warps
+constexpr int kTB = 4;  // tokens per x load batch in the scoring loop
+
 __device__ __forceinline__ void sbar(int nsw) {
   asm volatile("bar.sync 2, %0;" ::"r"(nsw * 32) : "memory");
 }
@@ -586,10 +590,10 @@ __device__ void score_experts(Smem& s, const DecodeParams& p, int sw) {
         v0[u] = ok ? __ldg(w0 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
         v1[u] = ok && has1 ? __ldg(w1 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      for (int t0 = 0; t0 < d.T; t0 += 2) {
-        uint2 xv[2][4];
+      for (int t0 = 0; t0 < d.T; t0 += kTB) {
+        uint2 xv[kTB][4];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < kTB; ++j) {
           const int t = min(t0 + j, d.T - 1);
           const uint2* xr = reinterpret_cast<const uint2*>(p.x + (size_t)t * d.H + sl * kw);
 #pragma unroll
@@ -599,7 +603,7 @@ __device__ void score_experts(Smem& s, const DecodeParams& p, int sw) {
           }
         }
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < kTB; ++j) {
           const int t = t0 + j;
           if (t >= d.T) break;
           float a0 = 0.f, a1 = 0.f;
@@ -647,14 +651,15 @@ __device__ void score_experts(Smem& s, const DecodeParams& p, int sw) {
 __device__ bool router_phase(Smem& s, const DecodeParams& p) {
   const Dims& d = p.d;
   const int tid = threadIdx.x - kRtr0 * 32, lane = tid & 31, warp = tid >> 5;
-  for (int e = tid; e < d.E; e += kRW * 32) s.bias_s[e] = __ldg(p.router_bias + e);
   score_experts(s, p, warp);
-  // publish this CTA's logits, then (off the logits' critical path) the
-  // interleaved x, then wait for everybody's logits
+  // publish this CTA's logits and wait for everybody's; the bias (needed only
+  // for the ranking) arrives meanwhile
   if (tid == 0) {
     __threadfence();
     atomicAdd(&p.sync[0], 1u);
+    mbar_arrive(&s.scored);
   }
+  for (int e = tid; e < d.E; e += kRW * 32) s.bias_s[e] = __ldg(p.router_bias + e);
   rbar();
   if (tid == 0) {
     s.flag = wait_counter(reinterpret_cast<const int*>(p.sync), (int)gridDim.x, p.r.err) ? 1 : 0;
@@ -746,6 +751,8 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
     if (nrec <= kMaxRecs)
       for (int j = tid - 32; j < nrec; j += (kRW - 1) * 32)
         s.trec[j] = task_record(task_at(s, d, c, first + j * G));
+    asm volatile("bar.sync 3, %0;" ::"n"((kRW - 1) * 32) : "memory");
+    if (tid == 32) mbar_arrive(&s.rec_ready);  // the producer decodes on the fly until then
   }
   if (warp == 0) {
     // stable placement, 32 items at a time: rank among equal experts in the
@@ -768,9 +775,9 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
       if (valid && rank == 0) s.run_s[e] += __popc(peers);
       __syncwarp();
     }
+    if (lane == 0) mbar_arrive(&s.route_ready);
   }
   rbar();
-  if (tid == 0) mbar_arrive(&s.route_ready);
   // one CTA also writes the routing out (the get-routing hook reads it)
   if (blockIdx.x == 0) {
     for (int i = tid; i < n; i += kRW * 32) {
@@ -831,6 +838,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.slot_free[i], 1);
     }
     mbar_init(&s.route_ready, 1);
+    mbar_init(&s.rec_ready, 1);
+    mbar_init(&s.scored, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -854,20 +863,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       const int nsub = p.nsub, gps = 8 * nsub;  // K groups per stage
-      int rec = 0, nrec = -1;
+      int rec = 0;     // tasks since the first routed one
+      int nrec = -2;   // records: -2 not ready yet, -1 none (too many), else their count
+      if (nsub == 2) dwait(&s.scored, 0, err);  // small batch: the router's loads go first
       for (int tau = blockIdx.x; !stop; tau += gridDim.x) {
         if (tau >= cnt.sh1 && !known) {
           if (!dwait(&s.route_ready, 0, err)) break;
           cnt.n_act = s.meta[0];
           cnt.r1 = s.meta[1];
           cnt.r2 = s.meta[2];
-          nrec = s.nrec;
           known = true;
         }
         Task t;
-        if (known && nrec >= 0) {
-          if (rec >= nrec) break;  // past the last task
-          t = task_of_record(d, s.trec[rec++]);
+        if (known) {
+          if (nrec == -2 && mbar_try_wait(&s.rec_ready, 0)) nrec = s.nrec;
+          if (nrec >= 0) {
+            if (rec >= nrec) break;  // past the last task
+            t = task_of_record(d, s.trec[rec]);
+          } else {
+            t = task_at(s, d, cnt, tau);
+          }
+          ++rec;
         } else {
           t = task_at(s, d, cnt, tau);
         }
