@@ -1253,13 +1253,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tile_last) {
         // this task completed a channel tile: combine it for every token
         asm volatile("fence.acq_rel.gpu;" ::: "memory");
-        const int n0 = ds.tile * kTile2;
-        for (int i = lane; i < d.T * kTile2; i += 32) {
-          const int tok = i / kTile2, n = n0 + (i - tok * kTile2);
-          float a = d.Is > 0 ? __ldcg(p.y + (size_t)(d.T * d.k + tok) * d.H + n) : 0.f;
-          for (int j = 0; j < d.k; ++j)
-            a = fmaf(s.wts_s[tok * d.k + j], __ldcg(p.y + (size_t)s.inv_s[tok * d.k + j] * d.H + n), a);
-          p.out[(size_t)tok * d.H + n] = f32_to_bf16_bits(a);
+        // lane (t4, q): channels n0 + 4q .. + 3 of tokens t4, t4 + 4, ...; all
+        // (k + 1) rows of a token are loaded before any is summed (the loop is
+        // bound by the latency of these L2 reads), the sum in slot order as
+        // everywhere
+        const int n = ds.tile * kTile2 + 4 * (lane & 7);
+        const float4* yv = reinterpret_cast<const float4*>(p.y + n);
+        const size_t rs = (size_t)d.H / 4;  // float4 per y row
+        for (int tok = lane >> 3; tok < d.T; tok += 4) {
+          float4 v[kMaxTopK];
+#pragma unroll
+          for (int j = 0; j < kMaxTopK; ++j)
+            if (j < d.k) v[j] = __ldcg(yv + (size_t)s.inv_s[tok * d.k + j] * rs);
+          float4 a = d.Is > 0 ? __ldcg(yv + (size_t)(d.T * d.k + tok) * rs) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < kMaxTopK; ++j) {
+            if (j >= d.k) break;
+            const float w = s.wts_s[tok * d.k + j];
+            a.x = fmaf(w, v[j].x, a.x);
+            a.y = fmaf(w, v[j].y, a.y);
+            a.z = fmaf(w, v[j].z, a.z);
+            a.w = fmaf(w, v[j].w, a.w);
+          }
+          const uint32_t lo = (uint32_t)f32_to_bf16_bits(a.x) | ((uint32_t)f32_to_bf16_bits(a.y) << 16);
+          const uint32_t hi = (uint32_t)f32_to_bf16_bits(a.z) | ((uint32_t)f32_to_bf16_bits(a.w) << 16);
+          *reinterpret_cast<uint2*>(p.out + (size_t)tok * d.H + n) = make_uint2(lo, hi);
         }
         if (lane == 0) p.tile_cnt[ds.tile] = 0;
       }
