@@ -85,7 +85,8 @@ constexpr int kWB = 2 * 16 * 512;            // sub-stage: 2 tiles x 16 rows x 5
 constexpr int kSB = 2 * 16 * 16;             // sub-stage: 2 tiles x 16 rows x 8 bf16 scales
 constexpr int kXSub = 8 * 256;               // one activation row of a sub-stage (8 groups bf16)
 constexpr int kMaxSub = 2;                   // sub-stages per stage at most
-constexpr int kWideRows = 4;                 // batches of at most this many tokens use 2 sub-stages
+constexpr int kGateRows = 4;                 // up to this many tokens the shared expert's
+                                             // stream waits for the router's loads
 constexpr int kSmemMax = 227 * 1024;         // opt-in shared memory of one CTA
 constexpr int kMaxPass = (kSmallT + kR - 1) / kR;  // passes per expert at most
 constexpr int kPairs = (kMaxExperts + 1) * kMaxPass;  // (expert, pass) counters
@@ -93,16 +94,20 @@ constexpr int kItems = kSmallT * kMaxTopK;
 constexpr int kMaxRecs = 512;                // a CTA's tasks after routing, kept as decoded records
 
 // Stage descriptor flags. The consumers read only this word of a stage's
-// descriptor: the K groups of the stage sit in bits 8-12 and the activation
-// rows in bits 13-16.
+// descriptor: the K groups of the stage sit in bits 8-12, the activation rows
+// in bits 13-16 and the offset of those rows in the activation pool, in
+// 128-byte units, in bits 17-26.
 // kPre: a gate/up stage, whose activation rows are the interleaved x.
 enum { kFirst = 1, kLast = 2, kEnd = 4, kShared = 8, kDown = 16, kPre = 32, kSwz = 64 };
-__host__ __device__ constexpr int stage_key(int flags, int gcnt, int nr) {
-  return flags | (gcnt << 8) | (nr << 13);
+__host__ __device__ constexpr int stage_key(int flags, int gcnt, int nr, int act) {
+  return flags | (gcnt << 8) | (nr << 13) | ((act >> 7) << 17);
 }
+// Bytes of one activation row of a stage of gcnt K groups (64 bytes off a
+// multiple of 128: the consumers' reads are conflict-free).
+__host__ __device__ constexpr int act_stride(int gcnt) { return gcnt * 256 + 64; }
 
 struct Desc {
-  int flags, g0, gcnt, ngroups, tile, r0, nr, rowA0, rowA1, cnt, pad[2];  // cnt: (expert, pass)
+  int flags, g0, gcnt, ngroups, tile, r0, nr, rowA0, rowA1, cnt, act, pad;  // cnt: (expert, pass)
 };
 
 struct Smem {
@@ -125,6 +130,7 @@ struct Smem {
   int meta[4];                          // n_act, routed gate/up tasks, routed down tasks
   uint2 trec[kMaxRecs];                 // this CTA's tasks from its first routed one on (task_record)
   int nrec;                             // records in trec, or -1 (too many: decode on the fly)
+  int apos[kMaxS];                      // producer: pool position of each in-flight stage's rows
   uint64_t full[kMaxS];
   uint64_t empty[kMaxS];
   uint64_t desc_ready[kMaxS];           // weight producer -> activation warp
@@ -162,9 +168,10 @@ struct DecodeParams {
   unsigned* sync;               // [4]: logits ticket, x-interleave ticket, exit ticket
   int scale_tma;
   int nst;                      // ring stages
-  int stage_bytes;              // bytes per stage (a multiple of 1024)
+  int stage_bytes;              // weight and scale bytes per stage (a multiple of 1024)
   int nsub;                     // sub-stages (8 K-groups each) per stage
-  int xs;                       // bytes per activation row of a stage (nsub groups of 8, + pad)
+  int pool_off;                 // the activation pool, after the ring (bytes from its start)
+  int pool_bytes;
 };
 
 struct Task {
@@ -865,7 +872,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nsub = p.nsub, gps = 8 * nsub;  // K groups per stage
       int rec = 0;     // tasks since the first routed one
       int nrec = -2;   // records: -2 not ready yet, -1 none (too many), else their count
-      if (nsub == 2) dwait(&s.scored, 0, err);  // small batch: the router's loads go first
+      // The activation pool is a FIFO in stage order: a stage's rows take
+      // [apos, apos + need) of an unbounded byte sequence, stored at that
+      // position modulo the pool (an allocation never wraps), and are freed
+      // when the stage is released. q counts stages, rel the released ones.
+      int q = 0, rel = 0, head = 0;
+      const int P = p.pool_bytes;
+      if (d.T <= kGateRows) dwait(&s.scored, 0, err);  // small batch: the router's loads go first
       for (int tau = blockIdx.x; !stop; tau += gridDim.x) {
         if (tau >= cnt.sh1 && !known) {
           if (!dwait(&s.route_ready, 0, err)) break;
@@ -898,12 +911,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             stop = true;
             break;
           }
+          rel = max(rel, q - nst + 1);  // the slot's previous stage is released
+          // room for nr activation rows in the pool: wait for the oldest
+          // stages' releases until they fit (a stage's release is the phase
+          // of its slot's empty barrier that completes when it is consumed)
+          const int need = (t.nr * act_stride(gcnt) + 127) & ~127;
+          int apos = head;
+          if (apos % P + need > P) apos += P - apos % P;
+          while (rel < q && apos + need - s.apos[rel % nst] > P) {
+            if (!dwait(&s.empty[rel % nst], (uint32_t)(rel / nst) & 1u, err)) {
+              stop = true;
+              break;
+            }
+            ++rel;
+          }
+          if (stop) break;
+          s.apos[stage] = apos;
+          head = apos + need;
           Desc& ds = s.desc[stage];
           const bool pre = !t.down;  // gate/up: the interleaved x rows
           ds.flags = stage_key((g0 == 0 ? kFirst : 0) | (g0 + gps >= t.ngroups ? kLast : 0) |
                                    (t.shared ? kShared : 0) | (t.down ? kDown : 0) |
                                    (pre ? kPre : 0) | (swz ? kSwz : 0),
-                               gcnt, t.nr);
+                               gcnt, t.nr, apos % P);
+          ds.act = apos % P;
           ds.g0 = g0;
           ds.gcnt = gcnt;
           ds.ngroups = t.ngroups;
@@ -913,10 +944,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ds.rowA0 = t.rowA0;
           ds.rowA1 = t.rowA1;
           ds.cnt = t.e * kMaxPass + t.pass;
-          // the activation warp copies nr rows into the stage; a TMA box always
-          // delivers its full size (out-of-range parts are zero-filled)
           // a box always delivers its full size (out-of-range parts are
-          // zero-filled); the activation warp copies nr rows into the stage
+          // zero-filled); the activation warp copies nr rows into the pool
           mbar_arrive_expect_tx(&s.full[stage], nsub * (kWB + (scale_tma ? kSB : 0)) + t.nr * gcnt * 256);
           const uint32_t st = smem_u32(stage_base + (size_t)stage * sb), ss = st + nsub * kWB;
           if (nsub == 2) {
@@ -942,6 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (scale_tma) tma_2d(ss, ts, &s.full[stage], g0, t.rowA0);
           }
           mbar_arrive(&s.desc_ready[stage]);
+          ++q;
           if (++stage == nst) {
             stage = 0;
             phase ^= 1u;
@@ -1052,7 +1082,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane < ds.nr) {
         const int r = ds.r0 + lane;
         const uint32_t slot =
-            smem_u32(stage_base + (size_t)stage * sb + p.nsub * (kWB + kSB) + lane * p.xs);
+            smem_u32(stage_base + p.pool_off + ds.act + lane * act_stride(ds.gcnt));
         const uint16_t* src;
         if (!down) {
           const int tok = (ds.flags & kShared) ? r - d.T * d.k : s.perm_s[r];
@@ -1082,7 +1112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nsub = p.nsub;
     const uint32_t tstride = nsub * (kWB / 2), sstride = nsub * (kSB / 2);  // per tile
     const uint32_t s_off = nsub * kWB + g * 16 * nsub + gw * 2;
-    const uint32_t xt_off = nsub * (kWB + kSB) + g * p.xs + gw * 256 + c * 16;  // transposed (xi, h)
+    const uint32_t pool0 = stage0 + p.pool_off;
+    const uint32_t xt_off = gw * 256 + c * 16;  // + row g of the stage's rows: transposed (xi, h)
     int stage = 0;
     uint32_t phase = 0;
     int tseq = 0;  // tasks finished (the same sequence for all consumer warps)
@@ -1096,13 +1127,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 4; ++i) acc[0][i] = acc[1][i] = 0.f;
       }
       const int gcnt = (key >> 8) & 31, nr = (key >> 13) & 15;
+      const uint32_t xrow = pool0 + (((uint32_t)key >> 17) << 7) + g * act_stride(gcnt);  // row g
       // sub-stage j: K groups 8 j .. 8 j + 7 of the stage; this warp takes group 8 j + gw
 #pragma unroll
       for (int j = 0; j < kMaxSub; ++j) {
         if (j >= nsub || 8 * j + gw >= gcnt) break;
         const uint32_t st = stage0 + stage * sb + j * (kWB / 2);  // + tile: this sub-stage's weights
         const uint32_t sj = stage0 + stage * sb + j * 16;  // + s_off: its scales
-        const uint32_t xj = stage0 + stage * sb + j * kXSub;  // + xt_off: its activations
+        const uint32_t xj = xrow + j * kXSub;  // + xt_off: its activations
         const uint32_t wo = (key & kSwz) ? w_off_s : w_off;
         uint4 wA[2], wB[2];
         float sc[2][2];  // [tile][row g / g + 8]
@@ -1309,27 +1341,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-// Ring geometry for a batch of T tokens: as many stages as fit (at most
-// kMaxS), each holding min(T, kR) activation rows. Up to kWideRows rows a
-// stage holds two sub-stages (16 K groups): half the per-stage hand-offs of
-// every warp role for the same bytes in flight.
-static void ring_of(int T, bool wide, int* nst, int* stage_bytes, int* nsub, int* xs) {
+// Ring geometry for a batch of T tokens. A stage holds only weights and
+// scales: 16 K groups (two sub-stages, 32 KB of weights) when the wide views
+// exist, else 8. The activation rows of the stages in flight share one FIFO
+// pool after the ring, sized for about two rows per stage (a pass holds up to
+// min(T, 8) rows; at 64 tokens most passes of a routed expert hold one or
+// two) and at least one full pass.
+static void ring_of(int T, bool wide, int* nst, int* stage_bytes, int* nsub, int* pool_off,
+                    int* pool_bytes) {
   const int rows = T < kR ? (T < 1 ? 1 : T) : kR;
-  *nsub = wide && rows <= kWideRows ? kMaxSub : 1;
-  *xs = *nsub * kXSub + 64;  // rows 64 bytes off a multiple of 128: conflict-free reads
-  *stage_bytes = (*nsub * (kWB + kSB) + rows * *xs + 1023) / 1024 * 1024;
-  const int n = (kSmemMax - kStageOff) / *stage_bytes;
-  *nst = n < kMaxS ? n : kMaxS;
+  *nsub = wide ? kMaxSub : 1;
+  const int gps = 8 * *nsub;
+  *stage_bytes = (*nsub * (kWB + kSB) + 1023) / 1024 * 1024;
+  const int maxact = (rows * act_stride(gps) + 127) & ~127;
+  const int typ = ((rows < 2 ? rows : 2) * act_stride(gps) + 127) & ~127;
+  const int avail = kSmemMax - kStageOff;
+  int n = avail / (*stage_bytes + typ);
+  if (n > kMaxS) n = kMaxS;
+  while (n > 1 && avail - n * *stage_bytes < maxact) --n;
+  *nst = n;
+  *pool_off = n * *stage_bytes;
+  *pool_bytes = avail - *pool_off;
+  if (*pool_bytes > (1 << 17)) *pool_bytes = 1 << 17;  // the stage key holds offsets below 128 KB
+  *pool_bytes &= ~127;
 }
 
 cudaError_t decode_setup(int* ctas_per_sm) {
   cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemMax);
   if (e != cudaSuccess) return e;
-  int nst, sb, nsub, xs;
-  ring_of(kSmallT, false, &nst, &sb, &nsub, &xs);
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_kernel, kThreads,
-                                                       kStageOff + nst * sb);
+                                                       kSmemMax);
 }
 
 size_t decode_counter_ints(int E, int H) { return (size_t)(E + 1) * kMaxPass + H / kTile2 + 4; }
@@ -1356,12 +1398,12 @@ cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& 
   p.tile_cnt = counters + (size_t)(d.E + 1) * kMaxPass;
   p.sync = reinterpret_cast<unsigned*>(p.tile_cnt + d.H / kTile2);
   p.scale_tma = w.scale_tma;
-  ring_of(d.T, w.wide != 0, &p.nst, &p.stage_bytes, &p.nsub, &p.xs);
+  ring_of(d.T, w.wide != 0, &p.nst, &p.stage_bytes, &p.nsub, &p.pool_off, &p.pool_bytes);
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kStageOff + p.nst * p.stage_bytes;
+  cfg.dynamicSmemBytes = kStageOff + p.pool_off + p.pool_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
