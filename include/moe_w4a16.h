@@ -199,10 +199,22 @@ int moe_w4a16_last_launches(moe_w4a16_handle* h, int32_t* count, const char** na
  * host threads) race with each other; the call clears the counters it needs
  * at zero on `stream` itself. cfg->max_tokens and cfg->flags are ignored;
  * x, out and the weights are device pointers as for moe_w4a16_forward.
- * Device-side error flags are not reported by this entry point. */
+ * The call returns once the work is enqueued; the device error word of the
+ * last call is read with moe_w4a16_noalloc_check_errors. The set-up is kept
+ * for the life of the process: after cudaDeviceReset on a device, this entry
+ * point must not be called on it again. */
 #define MOE_W4A16_NOALLOC_MAX_TOKENS 16
 int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint16_t* x, int32_t num_tokens,
                               const moe_w4a16_weights* w, uint16_t* out, void* stream);
+
+/* Device error flags of the last moe_w4a16_forward_noalloc call on the
+ * current device (the same bits as moe_w4a16_check_device_errors; 0 when the
+ * kernel's bounded waits all completed). No passage defines it. Synchronises
+ * `stream` (the stream that call used), then reads the word at the fixed
+ * start of the scratch array. *flags = 0 if no such call was made on this
+ * device. Returns MOE_W4A16_ERR_INVALID_ARG for a null flags pointer, a CUDA
+ * status for a failed synchronisation or copy. */
+int moe_w4a16_noalloc_check_errors(void* stream, uint32_t* flags);
 
 /* Pack signed 4-bit weights into the storage format of w13_q / w2_q.
  *

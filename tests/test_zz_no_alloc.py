@@ -52,7 +52,7 @@ def _compare(shape, T, bias=None):
         out = torch.full((T, shape.hidden), -1, dtype=torch.int16, device=DEV)
         moe.moe_w4a16_forward_noalloc(obj.cfg, x.data_ptr(), T, obj.weights, out.data_ptr(),
                                       stream)
-        torch.cuda.synchronize()
+        assert moe.moe_w4a16_noalloc_check_errors(stream) == 0
         _close(out.cpu().numpy(), ref)
     oracle = mc.oracle(layer)
     mc.check_output(out.cpu().numpy(), oracle["out"])

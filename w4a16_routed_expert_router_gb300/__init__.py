@@ -43,6 +43,7 @@ EXPORTS = (
     "moe_w4a16_last_launches",
     "moe_w4a16_status_string",
     "moe_w4a16_forward_noalloc",
+    "moe_w4a16_noalloc_check_errors",
     "moe_w4a16_pack_int4",
 )
 MOE_W4A16_NOALLOC_MAX_TOKENS = 16
@@ -100,6 +101,7 @@ def lib() -> ctypes.CDLL:
                                          ctypes.POINTER(ctypes.c_float), i32], ctypes.c_int),
             "moe_w4a16_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "moe_w4a16_forward_noalloc": ([cfgp, vp, i32, wp, vp, vp], ctypes.c_int),
+            "moe_w4a16_noalloc_check_errors": ([vp, u32p], ctypes.c_int),
             "moe_w4a16_pack_int4": ([vp, ctypes.c_int64, ctypes.c_int64, vp], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
@@ -160,6 +162,14 @@ def moe_w4a16_forward_noalloc(cfg: moe_w4a16_config, x_ptr: int, num_tokens: int
     _check(lib().moe_w4a16_forward_noalloc(ctypes.byref(cfg), x_ptr, num_tokens,
                                            ctypes.byref(weights), out_ptr, stream),
            "moe_w4a16_forward_noalloc")
+
+
+def moe_w4a16_noalloc_check_errors(stream: int = 0) -> int:
+    """Device error flags of the last no-allocation forward on this device."""
+    v = ctypes.c_uint32(0)
+    _check(lib().moe_w4a16_noalloc_check_errors(stream, ctypes.byref(v)),
+           "moe_w4a16_noalloc_check_errors")
+    return int(v.value)
 
 
 def moe_w4a16_pack_int4(q):

@@ -952,10 +952,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // wide views: 16 K groups of both tiles in one box
             if (!t.down) {
               tma_5d(st, tm, &s.full[stage], 0, 0, t.tile * kTile1, g0 / 8, half);
-              if (scale_tma) tma_3d(ss, ts, &s.full[stage], g0, t.tile * kTile1, half);
+              if (scale_tma) tma_4d(ss, ts, &s.full[stage], 0, t.tile * kTile1, g0 / 8, half);
             } else {
               tma_5d(st, tm, &s.full[stage], 0, 0, 0, g0 / 8, t.rowA0 / 16);
-              if (scale_tma) tma_2d(ss, ts, &s.full[stage], g0, t.rowA0);
+              if (scale_tma) tma_4d(ss, ts, &s.full[stage], 0, 0, g0 / 8, t.rowA0 / 16);
             }
           } else if (!t.down) {
             if (swz)
@@ -1108,10 +1108,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t w_off_s =
         g * 512 + seg * 128 + (((((uint32_t)(gw & 1) << 2) | c) ^ (seg | ((uint32_t)(g & 1) << 2))) << 4);
     // a stage is [tile][sub-stage][16 rows][512 B] of weights, then the
-    // scales [tile][16 rows][8 nsub], then the activation rows
+    // scales [tile][sub-stage][16 rows][8]; the activation rows are in the pool
     const int nsub = p.nsub;
     const uint32_t tstride = nsub * (kWB / 2), sstride = nsub * (kSB / 2);  // per tile
-    const uint32_t s_off = nsub * kWB + g * 16 * nsub + gw * 2;
+    const uint32_t s_off = nsub * kWB + g * 16 + gw * 2;
     const uint32_t pool0 = stage0 + p.pool_off;
     const uint32_t xt_off = gw * 256 + c * 16;  // + row g of the stage's rows: transposed (xi, h)
     int stage = 0;
@@ -1133,7 +1133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < kMaxSub; ++j) {
         if (j >= nsub || 8 * j + gw >= gcnt) break;
         const uint32_t st = stage0 + stage * sb + j * (kWB / 2);  // + tile: this sub-stage's weights
-        const uint32_t sj = stage0 + stage * sb + j * 16;  // + s_off: its scales
+        const uint32_t sj = stage0 + stage * sb + j * 256;  // + s_off: its scales
         const uint32_t xj = xrow + j * kXSub;  // + xt_off: its activations
         const uint32_t wo = (key & kSwz) ? w_off_s : w_off;
         uint4 wA[2], wB[2];
@@ -1144,7 +1144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           wB[tl] = lds128(st + tl * tstride + wo + 8 * 512);
           if (scale_tma) {
             sc[tl][0] = bf16_bits_to_f32(lds16(sj + tl * sstride + s_off));
-            sc[tl][1] = bf16_bits_to_f32(lds16(sj + tl * sstride + s_off + 8 * 16 * nsub));
+            sc[tl][1] = bf16_bits_to_f32(lds16(sj + tl * sstride + s_off + 8 * 16));
           } else {
             const Desc& dd = s.desc[stage];
             const uint16_t* scl = (key & kDown) ? ((key & kShared) ? p.s2_shared : p.s2_routed)

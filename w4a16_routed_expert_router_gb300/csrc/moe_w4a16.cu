@@ -308,7 +308,10 @@ int encode_decode_s2(CUtensorMap* m, const void* base, long long rows, int K) {
 // of a block stay 512 bytes apart.
 //  gate/up: {32 words, 4 segments, I' rows, K/1024, 2E' halves}, box {32, 4, 16, 2, 2}
 //  down:    {32 words, 4 segments, 16 rows, K/1024, E'H/16 tiles}, box {32, 4, 16, 2, 2}
-//  scales:  {K/128, I', 2E'} box {16, 16, 2}; {K/128, rows} box {16, 32}
+//  scales:  {8 groups, I' rows, K/1024, 2E' halves}, box {8, 16, 2, 2};
+//           {8 groups, 16 rows, K/1024, E'H/16 tiles}, box {8, 16, 2, 2}: laid out
+//           [tile][half of the 16 groups][16 rows][8] like the weights, rows
+//           16 bytes apart as in the narrow views (conflict-free reads)
 // An encode the driver refuses leaves the caller on the narrow views.
 int encode_decode_w13_wide(CUtensorMap* m, const void* base, int halves, int inter, int K) {
   const cuuint64_t dims[5] = {32, 4, (cuuint64_t)inter, (cuuint64_t)(K / 1024), (cuuint64_t)halves};
@@ -325,17 +328,19 @@ int encode_decode_w2_wide(CUtensorMap* m, const void* base, long long rows, int 
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, nullptr);
 }
 int encode_decode_s13_wide(CUtensorMap* m, const void* base, int halves, int inter, int K) {
-  const cuuint64_t dims[3] = {(cuuint64_t)(K / kGroup), (cuuint64_t)inter, (cuuint64_t)halves};
-  const cuuint64_t str[2] = {(cuuint64_t)(K / kGroup) * 2, (cuuint64_t)inter * (K / kGroup) * 2};
-  const cuuint32_t box[3] = {16, 16, 2};
-  return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, base, dims, str, box,
+  const cuuint64_t ng = (cuuint64_t)(K / kGroup);
+  const cuuint64_t dims[4] = {8, (cuuint64_t)inter, (cuuint64_t)(K / 1024), (cuuint64_t)halves};
+  const cuuint64_t str[3] = {ng * 2, 16, (cuuint64_t)inter * ng * 2};
+  const cuuint32_t box[4] = {8, 16, 2, 2};
+  return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, base, dims, str, box,
                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, nullptr);
 }
 int encode_decode_s2_wide(CUtensorMap* m, const void* base, long long rows, int K) {
-  const cuuint64_t dims[2] = {(cuuint64_t)(K / kGroup), (cuuint64_t)rows};
-  const cuuint64_t str[1] = {(cuuint64_t)(K / kGroup) * 2};
-  const cuuint32_t box[2] = {16, 32};
-  return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dims, str, box,
+  const cuuint64_t ng = (cuuint64_t)(K / kGroup);
+  const cuuint64_t dims[4] = {8, 16, (cuuint64_t)(K / 1024), (cuuint64_t)(rows / 16)};
+  const cuuint64_t str[3] = {ng * 2, 16, 16 * ng * 2};
+  const cuuint32_t box[4] = {8, 16, 2, 2};
+  return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, base, dims, str, box,
                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, nullptr);
 }
 
@@ -915,14 +920,14 @@ NoAllocLayout noalloc_plan(const moe_w4a16_config& c, int T) {
       (E + 2) * 4,                                       // 8 task2
       Tz * k * 4,                                        // 9 perm
       Tz * k * 4,                                        // 10 inv
-      4,                                                 // 11 err
+      0,                                                 // 11 (the error word sits at offset 0)
       decode_counter_ints(c.num_experts, c.hidden) * 4,  // 12 counters
       rows * hstride * 2,                                // 13 h
       rows * H * 4,                                      // 14 y
       Tz * H * 2,                                        // 15 x interleaved
   };
   NoAllocLayout L;
-  size_t o = 0;
+  size_t o = 256;  // the first 256 bytes: the device error word, at a fixed offset
   for (size_t i = 0; i < sizeof(sizes) / sizeof(sizes[0]); ++i) {
     L.off[i] = o;
     o += align256(sizes[i]);
@@ -932,6 +937,28 @@ NoAllocLayout noalloc_plan(const moe_w4a16_config& c, int T) {
 }
 
 }  // namespace
+
+extern "C" int moe_w4a16_noalloc_check_errors(void* stream, uint32_t* flags) {
+  if (!flags) return MOE_W4A16_ERR_INVALID_ARG;
+  *flags = 0;
+  int dev = -1, st;
+  if ((st = cuda_status(cudaGetDevice(&dev))) != MOE_W4A16_OK) return st;
+  if (dev < 0 || dev >= kMaxDevices) return MOE_W4A16_ERR_NO_DEVICE;
+  NoAllocDevice nd;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    nd = g_noalloc[dev];
+  }
+  if (!nd.ready) return MOE_W4A16_OK;  // no call on this device yet
+  if ((st = cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)))) != MOE_W4A16_OK)
+    return st;
+  unsigned v = 0;
+  if ((st = cuda_status(cudaMemcpy(&v, nd.scratch, sizeof(v), cudaMemcpyDeviceToHost))) !=
+      MOE_W4A16_OK)
+    return st;
+  *flags = v;
+  return MOE_W4A16_OK;
+}
 
 extern "C" int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint16_t* x,
                                          int32_t T, const moe_w4a16_weights* w, uint16_t* out,
@@ -999,7 +1026,7 @@ extern "C" int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint
   r.task3 = nullptr;
   r.task4 = nullptr;
   r.xperm = nullptr;
-  r.err = reinterpret_cast<unsigned*>(b + L.off[11]);
+  r.err = reinterpret_cast<unsigned*>(b);
   int* counters = reinterpret_cast<int*>(b + L.off[12]);
   uint16_t* hbuf = reinterpret_cast<uint16_t*>(b + L.off[13]);
   float* ybuf = reinterpret_cast<float*>(b + L.off[14]);
