@@ -73,12 +73,15 @@ def layer_work(shape, counts):
             "bytes": w13_bytes + w2_bytes + act + router, "flops": flops}
 
 
-def kernel_work(name, shape, work):
+def kernel_work(name, shape, work, y_bytes=None):
     """Algorithmic DRAM bytes and useful FLOPs of one launch of a kernel.
 
     Bytes: the INT4 weights and scales of the experts hit, plus each
     activation operand read once and each result written once. FLOPs: 2 per
     multiply-add of the layer's own arithmetic (no padding, no re-reads).
+    y, the per-expert down output, is bf16 (2 bytes) after the tensor-core
+    down GEMM and fp32 (4) after the GEMV one; y_bytes says which one the
+    combine read (default: bf16).
     """
     T, H, E, k, I, Is = (shape.tokens, shape.hidden, shape.experts, shape.top_k, shape.inter,
                          shape.shared_inter)
@@ -94,12 +97,14 @@ def kernel_work(name, shape, work):
         # activations counted once (T rows); the expert-ordered copy of x the
         # GEMM reads instead is an implementation choice (implementation_bytes)
         return work["w13_bytes"] + T * H * 2 + hrows * 2, f13
-    if name.startswith("gemv_down") or name.startswith("tc_down"):
+    if name.startswith("gemv_down"):
         return work["w2_bytes"] + hrows * 2 + rows * H * 4, f2
+    if name.startswith("tc_down"):
+        return work["w2_bytes"] + hrows * 2 + rows * H * 2, f2
     if name.startswith("route") or name.startswith("router"):
         return work["router_bytes"] + T * H * 2 * 2, 2 * T * E * H
     if name == "combine":
-        return rows * H * 4 + T * H * 2, 2 * T * k * H
+        return rows * H * (2 if y_bytes is None else y_bytes) + T * H * 2, 2 * T * k * H
     return 0, 0
 
 
@@ -113,10 +118,10 @@ def implementation_bytes(name, shape):
     return 0
 
 
-def roofline(name, shape, work, seconds, pk):
+def roofline(name, shape, work, seconds, pk, y_bytes=None):
     """Roofline entry of one kernel: whichever of the HBM and bf16 tensor
     bounds is slower for its algorithmic work decides the bound."""
-    nbytes, flops = kernel_work(name, shape, work)
+    nbytes, flops = kernel_work(name, shape, work, y_bytes)
     extra = implementation_bytes(name, shape)
     t_mem = nbytes / (pk["hbm_gbs"] * 1e9)
     t_mma = flops / (pk["bf16_tflops"] * 1e12)
@@ -438,7 +443,8 @@ class Bench:
         prof.close()
 
         pk = peaks()
-        roof = roofline(dominant, shape, work, kernel_avg[dominant] / 1000.0, pk)
+        y_bytes = 4 if any(n.startswith("gemv_down") for n in kernel_avg) else 2
+        roof = roofline(dominant, shape, work, kernel_avg[dominant] / 1000.0, pk, y_bytes)
         roof["traffic"] = profiled_traffic(dominant, shape.name)
         layer_roof_s = max(work["bytes"] / (pk["hbm_gbs"] * 1e9),
                            work["flops"] / (pk["bf16_tflops"] * 1e12))

@@ -108,12 +108,15 @@ cudaError_t tc_setup(int* ctas_per_sm);
 cudaError_t launch_tc_gate_up(const Dims& d, const Routing& r, const TcWeights& w,
                               const CUtensorMap& xmap, uint16_t* h, int hstride, int grid,
                               cudaStream_t s, LaunchLog& log);
-// down: hmap is the same kind of view {hstride, rows} of h; writes y rows
+// down: hmap is the same kind of view {hstride, rows} of h; writes y rows in bf16
 cudaError_t launch_tc_down(const Dims& d, const Routing& r, const TcWeights& w,
-                           const CUtensorMap& hmap, float* y, int grid, cudaStream_t s,
+                           const CUtensorMap& hmap, uint16_t* y, int grid, cudaStream_t s,
                            LaunchLog& log);
 
+// y fp32 (the GEMV engine's) or bf16 (the tensor-core engine's)
 cudaError_t launch_combine(const Dims& d, const Routing& r, const float* y, uint16_t* out,
+                           cudaStream_t s, LaunchLog& log);
+cudaError_t launch_combine(const Dims& d, const Routing& r, const uint16_t* y, uint16_t* out,
                            cudaStream_t s, LaunchLog& log);
 
 }  // namespace moe

@@ -730,9 +730,13 @@ int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t T, const m
     if ((e = launch_tc_gate_up(d, h->r, t1, h->xmap, h->h, h->hstride, h->tc_grid, s, h->log)) !=
         cudaSuccess)
       return cuda_status(e);
-    if ((e = launch_tc_down(d, h->r, t2, h->hmap, h->y, h->tc_grid, s, h->log)) != cudaSuccess)
+    // y in bf16: half the bytes of its round trip through HBM (written here, read
+    // once by the combine); one more rounding per expert output, inside the
+    // layer's output tolerance
+    uint16_t* ybf = reinterpret_cast<uint16_t*>(h->y);
+    if ((e = launch_tc_down(d, h->r, t2, h->hmap, ybf, h->tc_grid, s, h->log)) != cudaSuccess)
       return cuda_status(e);
-    if ((e = launch_combine(d, h->r, h->y, out, s, h->log)) != cudaSuccess) return cuda_status(e);
+    if ((e = launch_combine(d, h->r, ybf, out, s, h->log)) != cudaSuccess) return cuda_status(e);
     h->last_T = T;
     return MOE_W4A16_OK;
   }

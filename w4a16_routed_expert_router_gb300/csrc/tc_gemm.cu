@@ -34,7 +34,8 @@
 //              layout tcgen05 reads; each thread fetches its row's group scale
 //              one group ahead with a plain load.
 //   warps 11-26 epilogue: tcgen05.ld of the accumulator (four warps per TMEM
-//              lane quarter, 16-column chunks), SwiGLU -> bf16 h, or fp32 y.
+//              lane quarter, 16-column chunks), SwiGLU -> bf16 h, or bf16 y (the
+//              combine reads y once; bf16 halves both sides of that round trip).
 // The activation operand (x rows in expert order, or h) is stored with each 8
 // consecutive values in the order (0,4)(1,5)(2,6)(3,7); the dequantiser emits
 // the weights in that same order, so no shuffle is needed on either side.
@@ -103,7 +104,7 @@ struct TcParams {
   const uint16_t* scale_shared;
   uint16_t* hout;                // gate/up: h [T*k + T, hstride], interleaved
   int hstride;
-  float* yout;                   // down: y [T*k + T, H]
+  uint16_t* yout;                // down: y [T*k + T, H] bf16
 };
 
 // q * scale for the two codes of int4_pair_to_bf16x2 (one bf16 rounding)
@@ -432,12 +433,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               hp[(size_t)j * p.hstride] = f32_to_bf16_bits(__fdividef(g, 1.0f + __expf(-g)) * v1[j]);
             }
         } else {
-          float* yr = p.yout + (size_t)(t.brow0 + c0) * d.H + t.chan0 + ch;
+          uint16_t* yr = p.yout + (size_t)(t.brow0 + c0) * d.H + t.chan0 + ch;
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             if (j < cn) {
-              yr[(size_t)j * d.H] = v0[j];
-              yr[(size_t)j * d.H + 128] = v1[j];
+              yr[(size_t)j * d.H] = f32_to_bf16_bits(v0[j]);
+              yr[(size_t)j * d.H + 128] = f32_to_bf16_bits(v1[j]);
             }
         }
       }
@@ -499,7 +500,7 @@ cudaError_t launch_tc_gate_up(const Dims& d, const Routing& r, const TcWeights& 
 }
 
 cudaError_t launch_tc_down(const Dims& d, const Routing& r, const TcWeights& w,
-                           const CUtensorMap& hmap, float* y, int grid, cudaStream_t s,
+                           const CUtensorMap& hmap, uint16_t* y, int grid, cudaStream_t s,
                            LaunchLog& log) {
   TcParams p{};
   p.d = d;
