@@ -12,7 +12,9 @@
 //
 //   [gate/up shared | gate/up routed | down shared | down routed]
 //
-// CTA b takes tasks b, b + G, b + 2G, ... (G = one CTA per SM). A task covers
+// (above 4 tokens the shared down tasks move ahead of the routed ones, see
+// task_at). CTA b takes tasks b, b + G, b + 2G, ... (G = one CTA per SM). A
+// task covers
 // two 16-row weight tiles (16 gate + 16 up channels, or 32 down channels) of
 // one expert over all of K, for one pass of <= 8 rows of that expert.
 //
@@ -383,18 +385,35 @@ __device__ __forceinline__ int find_active(const int* pre, int n_act, int tau) {
 // first part needs no routing; every CTA takes all its gate/up tasks before
 // its down tasks, and the shared down work sits between the two routed halves
 // so that the routed gate/up stream starts as soon as the routing is known.
+// Above kGateRows tokens the shared expert's down tasks come right after its
+// gate/up tasks, inside the routing window: their stages hold a full pass of
+// 8 activation rows each, so the pool takes them one at a time, which the
+// routing hides but the routed stream would not. At smaller batches they sit
+// between the routed halves, where their h is long ready.
+__device__ __forceinline__ bool shared_down_first(const Dims& d) { return d.T > kGateRows; }
+__device__ __forceinline__ int pre_routing_tasks(const Dims& d, const Counts& c) {
+  return c.sh1 + (shared_down_first(d) ? c.sh2 : 0);
+}
+
 __device__ __forceinline__ Task task_at(const Smem& s, const Dims& d, const Counts& c, int tau) {
   const int sh0 = d.T * d.k, sh1 = d.T * d.k + d.T;
+  const bool early = shared_down_first(d);
   if (tau < c.sh1) return make_task(d, false, true, d.E, sh0, sh1, tau);
   tau -= c.sh1;
+  if (early) {
+    if (tau < c.sh2) return make_task(d, true, true, d.E, sh0, sh1, tau);
+    tau -= c.sh2;
+  }
   if (tau < c.r1) {
     const int a = find_active(s.pre1, c.n_act, tau);
     const int e = s.active[a];
     return make_task(d, false, false, e, s.offsets[e], s.offsets[e + 1], tau - s.pre1[a]);
   }
   tau -= c.r1;
-  if (tau < c.sh2) return make_task(d, true, true, d.E, sh0, sh1, tau);
-  tau -= c.sh2;
+  if (!early) {
+    if (tau < c.sh2) return make_task(d, true, true, d.E, sh0, sh1, tau);
+    tau -= c.sh2;
+  }
   if (tau < c.r2) {
     const int a = find_active(s.pre2, c.n_act, tau);
     const int e = s.active[a];
@@ -752,7 +771,8 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
     c.r2 = s.meta[2];
     const int b = blockIdx.x, G = gridDim.x;
     const int total = c.sh1 + c.r1 + c.sh2 + c.r2;
-    const int first = c.sh1 <= b ? b : b + ((c.sh1 - b + G - 1) / G) * G;
+    const int npre = pre_routing_tasks(d, c);
+    const int first = npre <= b ? b : b + ((npre - b + G - 1) / G) * G;
     const int nrec = first < total ? (total - first + G - 1) / G : 0;
     if (tid == 32) s.nrec = nrec <= kMaxRecs ? nrec : -1;
     if (nrec <= kMaxRecs)
@@ -880,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int P = p.pool_bytes;
       if (d.T <= kGateRows) dwait(&s.scored, 0, err);  // small batch: the router's loads go first
       for (int tau = blockIdx.x; !stop; tau += gridDim.x) {
-        if (tau >= cnt.sh1 && !known) {
+        if (tau >= pre_routing_tasks(d, cnt) && !known) {
           if (!dwait(&s.route_ready, 0, err)) break;
           cnt.n_act = s.meta[0];
           cnt.r1 = s.meta[1];
@@ -1268,17 +1288,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!down) {
           asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.done1 + ds.cnt) : "memory");
         } else {
-          if (routed_down < 0) {
-            // a shared-expert down task can finish before the routing exists
-            routed_down = dwait(&s.route_ready, 0, err) ? s.meta[2] : 0;
-          }
-          const int per_tile = (cnt.sh2 + routed_down) / (d.H / kTile2);
+          // A shared-expert down task can finish before the routing exists;
+          // then it is not a tile's last (every tile has routed down tasks,
+          // and they need the routing), so it only counts itself.
+          if (routed_down < 0 && mbar_try_wait(&s.route_ready, 0)) routed_down = s.meta[2];
           int old;
           asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
                        : "=r"(old)
                        : "l"(p.tile_cnt + ds.tile)
                        : "memory");
-          tile_last = old == per_tile - 1;
+          tile_last = routed_down >= 0 && old == (cnt.sh2 + routed_down) / (d.H / kTile2) - 1;
         }
       }
       tile_last = __shfl_sync(0xffffffffu, tile_last, 0);
