@@ -163,7 +163,7 @@ struct DecodeParams {
   uint16_t* xi;                 // [T, H] bf16: x interleaved, chunks transposed (chunk_t)
   uint16_t* h;                  // [rows, hstride] bf16, interleaved, chunks transposed
   int hstride;
-  float* y;                     // [rows, H] fp32
+  uint16_t* y;                  // [rows, H] bf16: each expert's down output
   uint16_t* out;                // [T, H] bf16
   int* done1;                   // [(E + 1) * kMaxPass] gate/up tasks done per (expert, pass)
   int* tile_cnt;                // [H / 32] down tasks done per channel tile
@@ -1275,9 +1275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pos = (n & ~127) | (chunk_t((n >> 3) & 15) << 3) | ((n & 3) << 1) | ((n >> 2) & 1);
           p.h[orow * p.hstride + pos] = f32_to_bf16_bits(silu(f0[q]) * f1[q]);
         } else {
-          float* yr = p.y + orow * d.H + ds.tile * kTile2;
-          yr[row] = f0[q];
-          yr[16 + row] = f1[q];
+          uint16_t* yr = p.y + orow * d.H + ds.tile * kTile2;
+          yr[row] = f32_to_bf16_bits(f0[q]);
+          yr[16 + row] = f32_to_bf16_bits(f1[q]);
         }
       }
       // each lane publishes its own h / y stores before the warp's release-add
@@ -1304,31 +1304,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tile_last) {
         // this task completed a channel tile: combine it for every token
         asm volatile("fence.acq_rel.gpu;" ::: "memory");
-        // lane (t4, q): channels n0 + 4q .. + 3 of tokens t4, t4 + 4, ...; all
+        // lane (t8, q): channels n0 + 8q .. + 7 of tokens t8, t8 + 8, ...; all
         // (k + 1) rows of a token are loaded before any is summed (the loop is
         // bound by the latency of these L2 reads), the sum in slot order as
         // everywhere
-        const int n = ds.tile * kTile2 + 4 * (lane & 7);
-        const float4* yv = reinterpret_cast<const float4*>(p.y + n);
-        const size_t rs = (size_t)d.H / 4;  // float4 per y row
-        for (int tok = lane >> 3; tok < d.T; tok += 4) {
-          float4 v[kMaxTopK];
+        const int n = ds.tile * kTile2 + 8 * (lane & 3);
+        const uint4* yv = reinterpret_cast<const uint4*>(p.y + n);
+        const size_t rs = (size_t)d.H / 8;  // 16-byte chunks per y row
+        for (int tok = lane >> 2; tok < d.T; tok += 8) {
+          uint4 v[kMaxTopK];
 #pragma unroll
           for (int j = 0; j < kMaxTopK; ++j)
             if (j < d.k) v[j] = __ldcg(yv + (size_t)s.inv_s[tok * d.k + j] * rs);
-          float4 a = d.Is > 0 ? __ldcg(yv + (size_t)(d.T * d.k + tok) * rs) : make_float4(0.f, 0.f, 0.f, 0.f);
+          float a[8];
+          {
+            const uint4 sh = d.Is > 0 ? __ldcg(yv + (size_t)(d.T * d.k + tok) * rs) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t q4[4] = {sh.x, sh.y, sh.z, sh.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              a[2 * i] = __uint_as_float(q4[i] << 16);
+              a[2 * i + 1] = __uint_as_float(q4[i] & 0xffff0000u);
+            }
+          }
 #pragma unroll
           for (int j = 0; j < kMaxTopK; ++j) {
             if (j >= d.k) break;
             const float w = s.wts_s[tok * d.k + j];
-            a.x = fmaf(w, v[j].x, a.x);
-            a.y = fmaf(w, v[j].y, a.y);
-            a.z = fmaf(w, v[j].z, a.z);
-            a.w = fmaf(w, v[j].w, a.w);
+            const uint32_t q4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              a[2 * i] = fmaf(w, __uint_as_float(q4[i] << 16), a[2 * i]);
+              a[2 * i + 1] = fmaf(w, __uint_as_float(q4[i] & 0xffff0000u), a[2 * i + 1]);
+            }
           }
-          const uint32_t lo = (uint32_t)f32_to_bf16_bits(a.x) | ((uint32_t)f32_to_bf16_bits(a.y) << 16);
-          const uint32_t hi = (uint32_t)f32_to_bf16_bits(a.z) | ((uint32_t)f32_to_bf16_bits(a.w) << 16);
-          *reinterpret_cast<uint2*>(p.out + (size_t)tok * d.H + n) = make_uint2(lo, hi);
+          uint4 o;
+          o.x = (uint32_t)f32_to_bf16_bits(a[0]) | ((uint32_t)f32_to_bf16_bits(a[1]) << 16);
+          o.y = (uint32_t)f32_to_bf16_bits(a[2]) | ((uint32_t)f32_to_bf16_bits(a[3]) << 16);
+          o.z = (uint32_t)f32_to_bf16_bits(a[4]) | ((uint32_t)f32_to_bf16_bits(a[5]) << 16);
+          o.w = (uint32_t)f32_to_bf16_bits(a[6]) | ((uint32_t)f32_to_bf16_bits(a[7]) << 16);
+          *reinterpret_cast<uint4*>(p.out + (size_t)tok * d.H + n) = o;
         }
         if (lane == 0) p.tile_cnt[ds.tile] = 0;
       }
@@ -1396,7 +1410,7 @@ cudaError_t decode_setup(int* ctas_per_sm) {
 size_t decode_counter_ints(int E, int H) { return (size_t)(E + 1) * kMaxPass + H / kTile2 + 4; }
 
 cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& w, const uint16_t* x,
-                          uint16_t* xi, uint16_t* h, int hstride, float* y, uint16_t* out,
+                          uint16_t* xi, uint16_t* h, int hstride, uint16_t* y, uint16_t* out,
                           int* counters, int grid, cudaStream_t s, LaunchLog& log) {
   DecodeParams p{};
   p.d = d;

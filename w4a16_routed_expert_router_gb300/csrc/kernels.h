@@ -91,7 +91,7 @@ size_t decode_counter_ints(int E, int H);
 // xi: [T, H] bf16 scratch, x interleaved with its 16-byte chunks transposed
 // within each K group, written by the kernel itself.
 cudaError_t launch_decode(const Dims& d, const Routing& r, const DecodeWeights& w, const uint16_t* x,
-                          uint16_t* xi, uint16_t* h, int hstride, float* y, uint16_t* out,
+                          uint16_t* xi, uint16_t* h, int hstride, uint16_t* y, uint16_t* out,
                           int* counters, int grid, cudaStream_t s, LaunchLog& log);
 
 // Tensor-core (tcgen05) expert GEMMs for large batches.

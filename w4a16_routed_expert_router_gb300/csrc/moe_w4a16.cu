@@ -657,7 +657,8 @@ int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t T, const m
       h->dec_ready = true;
     }
     const DecodeWeights& dw = h->dec;
-    if ((e = launch_decode(d, h->r, dw, x, h->r.xperm, h->h, h->hstride, h->y, out,
+    if ((e = launch_decode(d, h->r, dw, x, h->r.xperm, h->h, h->hstride,
+                           reinterpret_cast<uint16_t*>(h->y), out,
                            h->counters, h->decode_grid, s, h->log)) != cudaSuccess)
       return cuda_status(e);
     h->last_T = T;
@@ -927,7 +928,7 @@ NoAllocLayout noalloc_plan(const moe_w4a16_config& c, int T) {
       0,                                                 // 11 (the error word sits at offset 0)
       decode_counter_ints(c.num_experts, c.hidden) * 4,  // 12 counters
       rows * hstride * 2,                                // 13 h
-      rows * H * 4,                                      // 14 y
+      rows * H * 2,                                      // 14 y (bf16)
       Tz * H * 2,                                        // 15 x interleaved
   };
   NoAllocLayout L;
@@ -1033,7 +1034,7 @@ extern "C" int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint
   r.err = reinterpret_cast<unsigned*>(b);
   int* counters = reinterpret_cast<int*>(b + L.off[12]);
   uint16_t* hbuf = reinterpret_cast<uint16_t*>(b + L.off[13]);
-  float* ybuf = reinterpret_cast<float*>(b + L.off[14]);
+  uint16_t* ybuf = reinterpret_cast<uint16_t*>(b + L.off[14]);
   uint16_t* xibuf = reinterpret_cast<uint16_t*>(b + L.off[15]);
   const int hstride = c.inter > c.shared_inter ? c.inter : c.shared_inter;
 
