@@ -88,6 +88,30 @@ def test_odd_shape_parity(odd, T):
     obj.close()
 
 
+# hidden and intermediate 1024 (every K a multiple of 1024: the decode
+# kernel's wide 32 KB stages) with 8 experts, top-2: at 64 tokens each expert
+# holds about 16 rows, so most stages carry a full pass of 8 activation rows
+# and the activation pool can hold only a few of them at once; ragged passes
+# at the other sizes. Above 64 tokens the tensor-core path.
+@pytest.fixture(scope="module")
+def wide():
+    shape = ms.MoeShape("wide1024", 16, 1024, 8, 2, 1024, 1024, 1008, 1008)
+    tensors = upload_layer(mc.weights_of(shape), DEV)[0]
+    return shape, tensors
+
+
+@pytest.mark.parametrize("T", [1, 3, 8, 17, 40, 64, 96])
+def test_wide_stage_parity(wide, T):
+    shape, tensors = wide
+    layer = mc.layer_with_tokens(shape, T)
+    ref = mc.oracle(layer)
+    obj = _layer_obj(layer, tensors, max_tokens=256)
+    out, rt = _run(obj, layer.x)
+    mc.check_routing(rt, ref, shape.experts)
+    mc.check_output(out, ref["out"])
+    obj.close()
+
+
 # a layer without a shared expert (shared_inter = 0): the decode kernel, the
 # tensor-core path and the GEMV engine
 @pytest.fixture(scope="module")
