@@ -330,17 +330,28 @@ def test_prefill8192_outputs_cover_every_active_expert(full):
     assert subset.size >= 256
 
 
-def test_zipf2048_repeated_forwards_are_bit_identical(full):
-    # Zipf routing puts ~90 experts with under 10 rows on the tensor-core path
-    # next to a 2048-row expert: tiny and full N-tiles in the same persistent
-    # schedule. Every forward of the same input must give the same bits.
-    shape = ms.CONFIGS["zipf2048"]
+@pytest.mark.parametrize("name,flags,kernel", [
+    ("zipf2048", 0, "tc_gate_up_swiglu"),
+    ("zipf2048", "gemv", "gemv_down"),
+    ("decode64", 0, "decode_fused"),
+])
+def test_repeated_forwards_are_bit_identical(full, name, flags, kernel):
+    # Every kernel with a TMA-filled stage ring read through generic loads
+    # (tensor-core dequantisers, GEMV and decode consumers) must release a
+    # stage only after a proxy fence; a missing one shows up as a few K blocks
+    # read from the next fill, differing from run to run. Zipf routing puts
+    # ~90 experts with under 10 rows next to a 2048-row expert: tiny and full
+    # N-tiles in the same persistent schedule. Every forward of the same input
+    # must give the same bits.
+    shape = ms.CONFIGS[name]
     layer = mc.layer_with_tokens(shape)
-    obj = _layer_obj(layer, full, shape.tokens, bias=layer.router_b)
+    f = moe.MOE_W4A16_FLAG_FORCE_GEMV if flags == "gemv" else flags
+    obj = _layer_obj(layer, full, shape.tokens, flags=f, bias=layer.router_b)
     x = upload_tokens(layer.x, DEV)
     first = obj.forward(x)
     torch.cuda.synchronize()
     first = first.cpu().numpy()
+    assert kernel in [n for n, _ in moe.moe_w4a16_last_launches(obj.handle)]
     for _ in range(40):
         again = obj.forward(x)
         torch.cuda.synchronize()

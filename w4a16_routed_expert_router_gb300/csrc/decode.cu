@@ -231,6 +231,13 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// generic shared-memory accesses of this thread before later async-proxy
+// (TMA, bulk copy) accesses of the same bytes, e.g. reads of a stage before
+// the release that lets the next fill overwrite it
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -1199,6 +1206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[tl][3] = fmaf(sc[tl][1], t4[tl][3], acc[tl][3]);
         }
       }
+      // the stage is refilled by TMA and bulk copies (async proxy) once
+      // released: order this thread's generic reads of it before that
+      fence_proxy_async_smem();
       if (key & kLast) {
         // end of a task: hand the partial sums to the slot's epilogue warp;
         // the stage's descriptor is copied before the stage is released

@@ -414,6 +414,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       acc[1][2] = fmaf(sc[3], tmp[2], acc[1][2]);
       acc[1][3] = fmaf(sc[3], tmp[3], acc[1][3]);
     }
+    // the stage's next fill is an async-proxy write (TMA, bulk copy): order
+    // this thread's generic reads of it before the release
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.empty[stage]);
     if (++stage == kGemvStages) {

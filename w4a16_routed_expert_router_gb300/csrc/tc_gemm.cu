@@ -55,12 +55,8 @@ constexpr int kThreads = 27 * 32;
 constexpr int kDqWarp0 = 3, kEpiWarp0 = 11;
 constexpr int kBK = 64;                               // K per block (one 128-byte swizzle atom)
 constexpr int kWStages = 4;
-// Three activation stages. With four (and the same weight and bf16 rings) the
-// outputs of tasks with few rows (N-tiles of up to 16 columns) differed from
-// run to run in some 32-channel quarters at 2048 Zipf-routed tokens (about one
-// forward in seven); with three, 400 repeated forwards were bit-identical and
-// the GEMMs ran within 2% of the four-stage time. A repeat-determinism test
-// covers this case.
+// Three activation stages: an activation tile takes about a microsecond to
+// arrive, three MMA K blocks' worth.
 constexpr int kBStages = 3;
 constexpr int kAbfStages = 2;
 constexpr int kInt4Tile = 128 * kBK / 2;              // 4 KB: 128 rows x 64 codes
@@ -379,8 +375,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(words[4]), "=r"(words[5]), "=r"(words[6]), "=r"(words[7])
                      : "r"(wsrc + (half0 ^ 16u)));
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.w_empty[wstage]);
         if (!warp_wait(&s.abf_empty[astage], aph ^ 1u, err)) {
           ok = false;
           break;
@@ -390,10 +384,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 8; ++j)
           sts128(dst + ((j ^ (row & 7)) << 4), dq_pair<0>(words[j], s2), dq_pair<1>(words[j], s2),
                  dq_pair<2>(words[j], s2), dq_pair<3>(words[j], s2));
-        // generic-proxy stores -> visible to the tensor core's async proxy
+        // one proxy fence for both directions: the bf16 stores become visible
+        // to the tensor core's async proxy, and the generic reads of the
+        // weight stage are ordered before its next TMA fill, so the weight
+        // stage is released only here. (Released right after the reads,
+        // without a fence, about one forward in six at 2048 Zipf-routed tokens
+        // had a few K blocks of some 32-row quarters dequantised from the
+        // next fill's weights.)
         fence_async_shared();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.abf_full[astage]);
+        if (lane == 0) {
+          mbar_arrive(&s.w_empty[wstage]);
+          mbar_arrive(&s.abf_full[astage]);
+        }
         if (++wstage == kWStages) {
           wstage = 0;
           wph ^= 1u;
