@@ -82,6 +82,9 @@ constexpr int kRtr0 = kEpi0 + kEW;           // first router warp
 constexpr int kThreads = (kCW + 2 + kEW + kRW) * 32;
 constexpr int kSW = kRW + kEW;               // warps that score experts (router + epilogue)
 constexpr int kR = 8;                        // rows per pass (MMA N)
+// above this many tokens the grid ranks them (one token per CTA) instead of
+// every CTA ranking all of them
+constexpr int kLocalRankT = 8;
 constexpr int kMaxS = 12;                    // ring stages at most (the count depends on T)
 constexpr int kWB = 2 * 16 * 512;            // sub-stage: 2 tiles x 16 rows x 512 B (8 K-groups)
 constexpr int kSB = 2 * 16 * 16;             // sub-stage: 2 tiles x 16 rows x 8 bf16 scales
@@ -679,6 +682,52 @@ __device__ void score_experts(Smem& s, const DecodeParams& p, int sw) {
   }
 }
 
+// Ranking spread over the grid, above kLocalRankT tokens: CTA b ranks tokens
+// b, b + G, ... (one router warp per token), publishes their ids and weights,
+// and reads everybody's back once all T tokens are ranked (a second grid
+// counter). Every CTA ranking all tokens itself would take T / 4 rankings per
+// router warp. Out of line on purpose: inlined, it changed the register
+// allocation of the whole kernel and cost the one-token forward about 4 us.
+__device__ __noinline__ bool rank_spread(const float* logits, int* ids, float* wts, unsigned* err,
+                                         unsigned* counter, const float* bias, int T, int E, int k,
+                                         int* s_ids, float* s_wts, int* s_counts, int* s_flag) {
+  const int tid = threadIdx.x - kRtr0 * 32, lane = tid & 31, warp = tid >> 5;
+  const int G = gridDim.x, b = blockIdx.x;
+  for (int t = b + warp * G; t < T; t += kRW * G) {
+    float lg[kPer];
+    load_logits(logits + (size_t)t * E, E, lane, lg);
+    int id;
+    float w;
+    warp_topk(lg, bias, E, k, lane, &id, &w);
+    if (lane < k) {
+      if (id < 0 || id >= E) {
+        atomicOr(err, kErrRange);
+        id = 0;
+      }
+      ids[t * k + lane] = id;
+      wts[t * k + lane] = w;
+    }
+  }
+  rbar();
+  if (tid == 0) {
+    const int mine = b < T ? (T - b + G - 1) / G : 0;
+    if (mine > 0) {
+      __threadfence();
+      atomicAdd(counter, (unsigned)mine);
+    }
+    *s_flag = wait_counter(reinterpret_cast<const int*>(counter), T, err) ? 1 : 0;
+  }
+  rbar();
+  if (!*s_flag) return false;
+  for (int i = tid; i < T * k; i += kRW * 32) {
+    const int id = __ldcg(ids + i);
+    s_ids[i] = id;
+    s_wts[i] = __ldcg(wts + i);
+    atomicAdd(&s_counts[id], 1);
+  }
+  return true;
+}
+
 // Router warps: score this CTA's experts, wait for every CTA's logits, then
 // compute the whole routing in shared memory. Returns false on timeout.
 __device__ bool router_phase(Smem& s, const DecodeParams& p) {
@@ -701,25 +750,31 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
   rbar();  // thread 0 acquired the counter; the barrier orders everybody's reads after it
   if (!s.flag) return false;
 
-  // ---- the routing of every token, in shared memory (the next token's logits
-  // are in flight while this one is ranked)
-  float lg[kPer], nx[kPer];
-  if (warp < d.T) load_logits(p.r.logits + (size_t)warp * d.E, d.E, lane, nx);
-  for (int t = warp; t < d.T; t += kRW) {
+  if (d.T > kLocalRankT) {
+    if (!rank_spread(p.r.logits, p.r.ids, p.r.wts, p.r.err, p.sync + 3, s.bias_s, d.T, d.E, d.k,
+                     s.ids_s, s.wts_s, s.counts_s, &s.flag))
+      return false;
+  } else {
+    // ---- the routing of every token, in shared memory (the next token's
+    // logits are in flight while this one is ranked)
+    float lg[kPer], nx[kPer];
+    if (warp < d.T) load_logits(p.r.logits + (size_t)warp * d.E, d.E, lane, nx);
+    for (int t = warp; t < d.T; t += kRW) {
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) lg[i] = nx[i];
-    if (t + kRW < d.T) load_logits(p.r.logits + (size_t)(t + kRW) * d.E, d.E, lane, nx);
-    int id;
-    float w;
-    warp_topk(lg, s.bias_s, d.E, d.k, lane, &id, &w);
-    if (lane < d.k) {
-      if (id < 0 || id >= d.E) {
-        atomicOr(p.r.err, kErrRange);
-        id = 0;
+      for (int i = 0; i < kPer; ++i) lg[i] = nx[i];
+      if (t + kRW < d.T) load_logits(p.r.logits + (size_t)(t + kRW) * d.E, d.E, lane, nx);
+      int id;
+      float w;
+      warp_topk(lg, s.bias_s, d.E, d.k, lane, &id, &w);
+      if (lane < d.k) {
+        if (id < 0 || id >= d.E) {
+          atomicOr(p.r.err, kErrRange);
+          id = 0;
+        }
+        s.ids_s[t * d.k + lane] = id;
+        s.wts_s[t * d.k + lane] = w;
+        atomicAdd(&s.counts_s[id], 1);
       }
-      s.ids_s[t * d.k + lane] = id;
-      s.wts_s[t * d.k + lane] = w;
-      atomicAdd(&s.counts_s[id], 1);
     }
   }
   rbar();
@@ -815,8 +870,10 @@ __device__ bool router_phase(Smem& s, const DecodeParams& p) {
   // one CTA also writes the routing out (the get-routing hook reads it)
   if (blockIdx.x == 0) {
     for (int i = tid; i < n; i += kRW * 32) {
-      p.r.ids[i] = s.ids_s[i];
-      p.r.wts[i] = s.wts_s[i];
+      if (d.T <= kLocalRankT) {  // else the ranking CTAs wrote them
+        p.r.ids[i] = s.ids_s[i];
+        p.r.wts[i] = s.wts_s[i];
+      }
       p.r.perm[i] = s.perm_s[i];
       p.r.inv[i] = s.inv_s[i];
     }
@@ -1373,6 +1430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
       p.sync[0] = 0u;
       p.sync[1] = 0u;
+      p.sync[3] = 0u;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
