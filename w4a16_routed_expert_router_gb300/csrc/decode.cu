@@ -170,7 +170,7 @@ struct DecodeParams {
   uint16_t* out;                // [T, H] bf16
   int* done1;                   // [(E + 1) * kMaxPass] gate/up tasks done per (expert, pass)
   int* tile_cnt;                // [H / 32] down tasks done per channel tile
-  unsigned* sync;               // [4]: logits ticket, x-interleave ticket, exit ticket
+  unsigned* sync;               // [4]: logits ticket, x-interleave ticket, exit ticket, ranked tokens
   int scale_tma;
   int nst;                      // ring stages
   int stage_bytes;              // weight and scale bytes per stage (a multiple of 1024)
@@ -1100,42 +1100,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int stage = 0;
     uint32_t phase = 0;
-    bool routed_known = false, pre_ready = false;
-    // poll every active (expert, pass) gate/up counter once (lanes in parallel)
-    // and record the finished ones; returns true when pair `want` is finished
-    auto poll_pairs = [&](int want) -> bool {
-      const int n_sh = d.Is > 0 ? passes_of(d.T) : 0;
-      const int n_act = routed_known ? s.meta[0] : 0;
-      for (int i = lane; i < n_sh + n_act * kMaxPass; i += 32) {
-        int e, pass, target;
-        if (i < n_sh) {
-          e = d.E;
-          pass = i;
-          target = d.Is / kTile1;
-        } else {
-          const int a = (i - n_sh) / kMaxPass;
-          e = s.active[a];
-          pass = (i - n_sh) - a * kMaxPass;
-          if (pass >= passes_of(s.offsets[e + 1] - s.offsets[e])) continue;
-          target = d.I / kTile1;
-        }
-        const int id = e * kMaxPass + pass;
-        if (s.pair_done[id >> 5] & (1u << (id & 31))) continue;
-        if (ld_acquire(p.done1 + id) >= target) atomicOr(&s.pair_done[id >> 5], 1u << (id & 31));
+    bool pre_ready = false;
+    // is the gate/up work of (expert, pass) `want` finished anywhere in the
+    // grid? One acquire load of its counter (lane 0), remembered in the CTA's
+    // bitmap. Polling every active pair at once cost the first down stage at
+    // 64 tokens a chain of ~49 dependent acquire loads per lane.
+    auto pair_ready = [&](int want) -> bool {
+      int ok = 0;
+      if (lane == 0) {
+        const int target = (want / kMaxPass == d.E ? d.Is : d.I) / kTile1;
+        ok = ld_acquire(p.done1 + want) >= target ? 1 : 0;
+        if (ok) s.pair_done[want >> 5] |= 1u << (want & 31);
       }
-      __syncwarp();
-      return (s.pair_done[want >> 5] >> (want & 31)) & 1u;
+      return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
     for (;;) {
       if (!__all_sync(0xffffffffu, dwait(&s.desc_ready[stage], phase, err))) break;
       const Desc ds = s.desc[stage];
       if (ds.flags & kEnd) break;
-      if (!routed_known && !(ds.flags & kShared)) routed_known = true;  // routing is in smem
       const bool down = (ds.flags & kDown) != 0;
-      if (down && !((s.pair_done[ds.cnt >> 5] >> (ds.cnt & 31)) & 1u)) {
+      // lane 0 writes the bitmap: its view decides, for the whole warp
+      if (down && !__shfl_sync(0xffffffffu, (s.pair_done[ds.cnt >> 5] >> (ds.cnt & 31)) & 1u, 0)) {
         // wait for the gate/up work of this (expert, pass) anywhere in the grid
         const uint64_t t0 = global_ns();
-        bool got = poll_pairs(ds.cnt);
+        bool got = pair_ready(ds.cnt);
         while (!got) {
           __nanosleep(128);
           if (aborted(err)) break;
@@ -1143,7 +1131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) atomicOr(err, kErrTimeout);
             break;
           }
-          got = poll_pairs(ds.cnt);
+          got = pair_ready(ds.cnt);
         }
         if (!got) break;
       }
