@@ -67,6 +67,7 @@
 //    resets the counters.
 #include "common.cuh"
 #include "kernels.h"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -480,7 +481,10 @@ __device__ __forceinline__ unsigned fkey(float f) {
 // lanes 0..k-1 return the chosen expert (descending sel, ties -> lower index)
 // and its renormalised unbiased score. A round is two warp reductions: the
 // largest selection key, then the lowest expert index among the lanes holding
-// it.
+// it. The sorted-list version (topk.cuh) gives the same results in ~0.6x the
+// time; rank_spread uses it, but inlined here it moves the register
+// allocation of the whole kernel and costs the one-token forward 2-3 us, so
+// the in-line ranking keeps this one.
 __device__ __forceinline__ void warp_topk(const float (&lg)[kPer], const float* bias, int E, int k,
                                           int lane, int* out_id, float* out_w) {
   float sc[kPer];
@@ -698,7 +702,7 @@ __device__ __noinline__ bool rank_spread(const float* logits, int* ids, float* w
     load_logits(logits + (size_t)t * E, E, lane, lg);
     int id;
     float w;
-    warp_topk(lg, bias, E, k, lane, &id, &w);
+    warp_topk_sorted<kMaxTopK>(lg, bias, E, k, lane, &id, &w);
     if (lane < k) {
       if (id < 0 || id >= E) {
         atomicOr(err, kErrRange);

@@ -18,6 +18,7 @@
 //    CTA's items stably with warp match/ballot.
 #include "common.cuh"
 #include "kernels.h"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -41,65 +42,11 @@ __device__ __forceinline__ void load_row(const float* logit_row, int E, int lane
 }
 
 // Warp-wide top-k of one token whose logits lane l holds for experts l, l+32,
-// ...; returns in lanes 0..k-1 the chosen expert (descending sel, ties ->
-// lower index) and its unbiased score.
+// ...: warp_topk_sorted (topk.cuh); returns in lanes 0..k-1 the chosen expert
+// (descending sel, ties -> lower index) and its renormalised unbiased score.
 __device__ __forceinline__ void warp_topk_regs(const float (&lg)[kPer], const float* bias, int E,
                                                int k, int lane, int* out_id, float* out_w) {
-  float sel[kPer], sc[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) {
-      const float l = lg[i];
-      const float s = 1.0f / (1.0f + expf(-l));
-      sc[i] = s;
-      sel[i] = s + bias[e];
-    } else {
-      sc[i] = 0.f;
-      sel[i] = -INFINITY;
-    }
-  }
-  float chosen_s = 0.f;
-  int chosen_e = -1;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = lane + 32 * i;
-      if (sel[i] > bv || (sel[i] == bv && e < be)) {
-        bv = sel[i];
-        be = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    // owner lane removes the winner and publishes its score
-    float ws = 0.f;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i)
-      if (lane + 32 * i == be) {
-        ws = sc[i];
-        sel[i] = -INFINITY;
-      }
-    ws = __shfl_sync(0xffffffffu, ws, be & 31);
-    if (lane == j) {
-      chosen_e = be;
-      chosen_s = ws;
-    }
-  }
-  // renormalise over the chosen experts in slot order (bias not included)
-  float sum = 0.f;
-  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, chosen_s, j);
-  *out_id = chosen_e;
-  *out_w = chosen_s / sum;
+  warp_topk_sorted<kMaxTopK>(lg, bias, E, k, lane, out_id, out_w);
 }
 
 // The same, reading the token's logits from a row in memory.
