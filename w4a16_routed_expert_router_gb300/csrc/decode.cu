@@ -592,7 +592,9 @@ __device__ __forceinline__ int4 rscan4(int4 v, int t, int4* scr, int4* total) {
 // when the batch is tiny (they are free until the first task ends, which
 // takes longer than scoring a few tokens; at larger batches scoring would hold
 // them up).
-__device__ __forceinline__ int scoring_warps(const Dims& d) { return d.T <= 4 ? kSW : kRW; }
+__device__ __forceinline__ int scoring_warps(const Dims& d) {
+  return d.T <= 4 ? kSW : (d.T <= kLocalRankT ? kRW : kSW + kCW);
+}
 
 // named barrier of the scoring warps
 constexpr int kTB = 4;  // tokens per x load batch in the scoring loop
@@ -612,12 +614,17 @@ __device__ __noinline__ void score_experts_impl(Smem& s, const Dims d, const flo
                                                float* logits, int sw) {
   const int nsw = scoring_warps(d);
   const int lane = threadIdx.x & 31, tid = sw * 32 + lane;
+  // more warps than slices: the warps of a slice split its token batches; a
+  // (slice, token) partial is computed the same way whichever warp takes it
+  const int share = nsw > kSW ? nsw / kSW : 1;
+  const int sl_first = nsw > kSW ? sw % kSW : sw, sl_step = nsw > kSW ? kSW : nsw;
+  const int t_first = (nsw > kSW ? sw / kSW : 0) * kTB;
   const int kw = d.H / kSW;   // K slice (a multiple of 16)
   const int nf = kw / 4;      // float4 of the slice
   for (int eb = blockIdx.x; eb < d.E; eb += 2 * gridDim.x) {
     const int e0 = eb, e1 = eb + gridDim.x;
     const bool has1 = e1 < d.E;
-    for (int sl = sw; sl < kSW; sl += nsw)
+    for (int sl = sl_first; sl < kSW; sl += sl_step)
     for (int f0 = 0; f0 < nf; f0 += 128) {
       const float4* w0 = reinterpret_cast<const float4*>(router_w + (size_t)e0 * d.H + sl * kw);
       const float4* w1 = reinterpret_cast<const float4*>(router_w + (size_t)(has1 ? e1 : e0) * d.H +
@@ -630,7 +637,7 @@ __device__ __noinline__ void score_experts_impl(Smem& s, const Dims d, const flo
         v0[u] = ok ? __ldg(w0 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
         v1[u] = ok && has1 ? __ldg(w1 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      for (int t0 = 0; t0 < d.T; t0 += kTB) {
+      for (int t0 = t_first; t0 < d.T; t0 += share * kTB) {
         uint2 xv[kTB][4];
 #pragma unroll
         for (int j = 0; j < kTB; ++j) {
@@ -1200,6 +1207,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     int tseq = 0;  // tasks finished (the same sequence for all consumer warps)
+    // above kLocalRankT tokens the consumers score experts first: the shared
+    // expert's 8-row stages come one at a time until the routing is known
+    if (scoring_warps(d) > kSW) score_experts(s, p, kSW + warp);
     float acc[2][4] = {};
     for (;;) {
       if (!dwait(&s.full[stage], phase, err)) break;
@@ -1446,7 +1456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // exist, else 8. The activation rows of the stages in flight share one FIFO
 // pool after the ring, sized for about two rows per stage (a pass holds up to
 // min(T, 8) rows; at 64 tokens most passes of a routed expert hold one or
-// two) and at least one full pass.
+// two) and at least one full pass, two above kGateRows tokens (the shared
+// expert's full passes come first there; three 32 KB stages and two passes
+// beat four stages and one at 64 tokens, 748 against 760 us).
 static void ring_of(int T, bool wide, int* nst, int* stage_bytes, int* nsub, int* pool_off,
                     int* pool_bytes) {
   const int rows = T < kR ? (T < 1 ? 1 : T) : kR;
@@ -1458,7 +1470,10 @@ static void ring_of(int T, bool wide, int* nst, int* stage_bytes, int* nsub, int
   const int avail = kSmemMax - kStageOff;
   int n = avail / (*stage_bytes + typ);
   if (n > kMaxS) n = kMaxS;
-  while (n > 1 && avail - n * *stage_bytes < maxact) --n;
+  // above kGateRows tokens the pool holds two full passes, so that two of the
+  // shared expert's 8-row stages are in flight before the routing is known
+  const int passes_in_pool = T > kGateRows ? 2 : 1;
+  while (n > 1 && avail - n * *stage_bytes < passes_in_pool * maxact) --n;
   *nst = n;
   *pool_off = n * *stage_bytes;
   *pool_bytes = avail - *pool_off;
