@@ -25,10 +25,12 @@ Parity status: ``e4m3_round``, ``quantize_blocks`` and ``w4a8_linear`` are
 pinned by ``tests/test_oracle_w4a8.py`` (brute force over all 256 e4m3 codes,
 hand-built ties and saturation, exact blocks, equality with the W4A16 weights
 on exactly representable inputs, a planted missing-scale bug, power-of-two
-invariance). ``swiglu_expert_w4a8`` and ``moe_forward_w4a8`` compose them; the
-composition (in particular that h is quantised before the down projection)
-is checked only by a loose bound against the W4A16 oracle: parity unpinned
-for those two.
+invariance). ``swiglu_expert_w4a8`` and ``moe_forward_w4a8`` are pinned by an
+independent brute-force composition on the tiny layer (its own nibble and
+bf16 decoding, nearest-code search over the enumerated e4m3 table, per-block
+scaled fp64 sums, every (token, slot) expert evaluated alone; the routing is
+the W4A16 oracle's, pinned by its own tests), and a variant without the fp8
+step on h is shown to differ.
 
 There is no W4A8 CUDA path yet; this oracle is the first step of that variant.
 """

@@ -165,3 +165,126 @@ def test_layer_close_to_w4a16_layer():
     np.testing.assert_array_equal(a8["ids"], a16["ids"])
     rel = np.linalg.norm(a8["out"] - a16["out"]) / np.linalg.norm(a16["out"])
     assert 1e-4 < rel < 0.08
+
+
+# ---------------------------------------------------------------------------
+# The expert and the layer against an independent brute-force composition:
+# its own nibble unpacking and bf16 decoding, the nearest-e4m3 search over the
+# enumerated code table (above), per-block scales from the fp32 amax, and the
+# per-block scaled dot products summed in fp64.
+
+def _bf16_value(bits):
+    b = (np.asarray(bits, dtype=np.uint32) * np.uint32(65536)).astype(np.uint32)
+    return b.view(np.float32).astype(np.float64)
+
+
+def _unpack_brute(words):
+    w = np.asarray(words, dtype=np.int64)
+    cols = [((w // (16 ** j)) % 16) - 8 for j in range(8)]     # code j at bits 4j..4j+3
+    return np.stack(cols, axis=-1).reshape(w.shape[0], -1)
+
+
+def _nearest_table(v, table, lsb):
+    """Vectorised brute force: nearest e4m3 value, ties to the even mantissa,
+    saturating at +-448."""
+    a = np.minimum(np.abs(v), 448.0)
+    pos = table[table >= 0]
+    plsb = lsb[table >= 0]
+    d = np.abs(pos[None, :] - a[:, None])
+    best = d.min(axis=1, keepdims=True)
+    tie = (d == best)
+    # among the tied grid points prefer the even mantissa, else the only one
+    pick = np.where(tie & (plsb[None, :] == 0), 1, 0) * 2 + tie.astype(int)
+    return np.copysign(pos[np.argmax(pick, axis=1)], v)
+
+
+def _quant_brute(rows32, table, lsb):
+    rows32 = np.asarray(rows32, dtype=np.float32)
+    R, K = rows32.shape
+    codes = np.zeros((R, K))
+    scales = np.zeros((R, K // 128))
+    for r in range(R):
+        for g in range(K // 128):
+            blk = rows32[r, 128 * g:128 * (g + 1)]
+            amax = np.float32(np.max(np.abs(blk)))
+            sc = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+            scales[r, g] = float(sc)
+            codes[r, 128 * g:128 * (g + 1)] = _nearest_table((blk / sc).astype(np.float64), table, lsb)
+    return codes, scales
+
+
+def _linear_brute(codes, scales, q, s_w):
+    R, K = codes.shape
+    N = q.shape[0]
+    y = np.zeros((R, N))
+    for g in range(K // 128):
+        part = codes[:, 128 * g:128 * (g + 1)] @ q[:, 128 * g:128 * (g + 1)].T.astype(np.float64)
+        y += part * scales[:, g:g + 1] * s_w[None, :, g]
+    return y
+
+
+def _expert_brute(x_rows, wts, table, lsb):
+    q13 = _unpack_brute(wts["w13_q"])
+    s13 = _bf16_value(wts["w13_s"])
+    q2 = _unpack_brute(wts["w2_q"])
+    s2 = _bf16_value(wts["w2_s"])
+    inter = q13.shape[0] // 2
+    xc, xs = _quant_brute(x_rows, table, lsb)
+    gu = _linear_brute(xc, xs, q13, s13)
+    g, u = gu[:, :inter], gu[:, inter:]
+    h = g / (1.0 + np.exp(-g)) * u
+    hc, hs = _quant_brute(h.astype(np.float32), table, lsb)
+    return _linear_brute(hc, hs, q2, s2)
+
+
+def test_expert_equals_brute_force_composition():
+    table, lsb = _e4m3_table()
+    shape = ms.CONFIGS["tiny16"]
+    layer = ms.make_layer(shape)
+    x = _bf16_value(layer.x[:6])
+    for wts in (layer.experts[3], layer.shared):
+        want = _expert_brute(x, wts, table, lsb)
+        got = w8.swiglu_expert_w4a8(x, wts)
+        np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12 * np.abs(want).max())
+
+
+def test_expert_brute_force_sees_the_h_quantisation():
+    """The brute-force expert without the fp8 step on h differs from the
+    oracle's expert (the composition pin would catch a dropped h quantisation)."""
+    table, lsb = _e4m3_table()
+    shape = ms.CONFIGS["tiny16"]
+    layer = ms.make_layer(shape)
+    x = _bf16_value(layer.x[:4])
+    wts = layer.experts[1]
+    q13, s13 = _unpack_brute(wts["w13_q"]), _bf16_value(wts["w13_s"])
+    q2, s2 = _unpack_brute(wts["w2_q"]), _bf16_value(wts["w2_s"])
+    xc, xs = _quant_brute(x, table, lsb)
+    gu = _linear_brute(xc, xs, q13, s13)
+    inter = q13.shape[0] // 2
+    h = gu[:, :inter] / (1.0 + np.exp(-gu[:, :inter])) * gu[:, inter:]
+    no_hq = h @ (q2 * np.repeat(s2, 128, axis=1)).T
+    got = w8.swiglu_expert_w4a8(x, wts)
+    assert not np.allclose(got, no_hq, rtol=1e-6, atol=1e-9)
+
+
+def test_layer_equals_brute_force_composition():
+    """moe_forward_w4a8 on the tiny layer: routing from the W4A16 oracle (pinned
+    by its own tests), every (token, slot) expert and the shared expert by the
+    brute force above, combined in slot order."""
+    table, lsb = _e4m3_table()
+    shape = ms.CONFIGS["tiny16"]
+    layer = ms.make_layer(shape)
+    got = w8.moe_forward_w4a8(layer.x, layer.router_w, layer.router_b, layer.experts,
+                              layer.shared, shape.top_k)
+    r = mo.route(layer.x, layer.router_w, layer.router_b, shape.experts, shape.top_k)
+    x = _bf16_value(layer.x)
+    want = np.zeros_like(x)
+    for t in range(x.shape[0]):
+        row = x[t:t + 1]
+        acc = _expert_brute(row, layer.shared, table, lsb)[0]
+        for j in range(shape.top_k):
+            e = int(r["ids"][t, j])
+            acc = acc + r["weights"][t, j] * _expert_brute(row, layer.experts[e], table, lsb)[0]
+        want[t] = acc
+    np.testing.assert_array_equal(got["ids"], r["ids"])
+    np.testing.assert_allclose(got["out"], want, rtol=1e-10, atol=1e-12 * np.abs(want).max())
