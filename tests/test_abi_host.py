@@ -36,6 +36,28 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
+HEADER_W4A8 = os.path.join(os.path.dirname(HEADER), "moe_w4a8.h")
+
+
+def test_w4a8_header_declares_the_binding_names(L):
+    names = sorted(set(re.findall(r"\b(moe_w4a8_[a-z0-9_]+)\s*\(", open(HEADER_W4A8).read())))
+    assert names == sorted(moe.EXPORTS_W4A8)
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_w4a8_calls_reject_bad_sizes_before_any_launch(L):
+    # K not a multiple of 128, N not a multiple of 16, negative rows: refused
+    # on the host with MOE_W4A8_INVALID_ARG (-1); rows == 0 is a no-op
+    assert L.moe_w4a8_quantize_blocks(None, 4, 100, None, None, None) == -1
+    assert L.moe_w4a8_quantize_blocks(None, -1, 128, None, None, None) == -1
+    assert L.moe_w4a8_quantize_blocks(None, 0, 128, None, None, None) == 0
+    assert L.moe_w4a8_linear(None, None, 4, 128, None, None, 20, None, None) == -1
+    assert L.moe_w4a8_linear(None, None, 4, 96, None, None, 16, None, None) == -1
+    assert L.moe_w4a8_linear(None, None, 0, 128, None, None, 16, None, None) == 0
+    assert L.moe_w4a8_linear(None, None, 4, 128, None, None, 16, None, None) == -1  # null pointers
+
+
 def _header_constants():
     """Every MOE_W4A16_* value the header defines (#define or enum member)."""
     text = open(HEADER).read()

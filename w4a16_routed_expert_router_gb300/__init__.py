@@ -46,6 +46,12 @@ EXPORTS = (
     "moe_w4a16_noalloc_check_errors",
     "moe_w4a16_pack_int4",
 )
+# the W4A8-FP8 building blocks (include/moe_w4a8.h)
+EXPORTS_W4A8 = (
+    "moe_w4a8_quantize_blocks",
+    "moe_w4a8_linear",
+)
+MOE_W4A8_OK = 0
 MOE_W4A16_NOALLOC_MAX_TOKENS = 16
 
 
@@ -103,6 +109,8 @@ def lib() -> ctypes.CDLL:
             "moe_w4a16_forward_noalloc": ([cfgp, vp, i32, wp, vp, vp], ctypes.c_int),
             "moe_w4a16_noalloc_check_errors": ([vp, u32p], ctypes.c_int),
             "moe_w4a16_pack_int4": ([vp, ctypes.c_int64, ctypes.c_int64, vp], ctypes.c_int),
+            "moe_w4a8_quantize_blocks": ([vp, i32, i32, vp, vp, vp], ctypes.c_int),
+            "moe_w4a8_linear": ([vp, vp, i32, i32, vp, vp, i32, vp, vp], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -184,6 +192,28 @@ def moe_w4a16_pack_int4(q):
     _check(lib().moe_w4a16_pack_int4(q.ctypes.data, rows, K, out.ctypes.data),
            "moe_w4a16_pack_int4")
     return out
+
+
+def moe_w4a8_quantize_blocks(x, codes, scales, stream: int = 0) -> None:
+    """fp8 e4m3 codes and fp32 scales of x (fp32 [rows, K] device tensor) per
+    row and 128-element block: codes uint8 [rows, K], scales fp32 [rows, K/128]."""
+    rows, K = x.shape
+    st = lib().moe_w4a8_quantize_blocks(x.data_ptr(), rows, K, codes.data_ptr(),
+                                        scales.data_ptr(), stream)
+    if st != MOE_W4A8_OK:
+        raise RuntimeError(f"moe_w4a8_quantize_blocks failed ({st})")
+
+
+def moe_w4a8_linear(codes, x_scales, w_q, w_s, y, stream: int = 0) -> None:
+    """y[r, n] = sum_g w_s[n, g] x_scales[r, g] sum_{k in g} q[n, k] codes[r, k]
+    (device tensors: codes uint8 [rows, K], x_scales fp32 [rows, K/128], w_q
+    int32/uint32 [N, K/8], w_s bf16 bits [N, K/128], y fp32 [rows, N])."""
+    rows, K = codes.shape
+    N = w_q.shape[0]
+    st = lib().moe_w4a8_linear(codes.data_ptr(), x_scales.data_ptr(), rows, K, w_q.data_ptr(),
+                               w_s.data_ptr(), N, y.data_ptr(), stream)
+    if st != MOE_W4A8_OK:
+        raise RuntimeError(f"moe_w4a8_linear failed ({st})")
 
 
 def moe_w4a16_get_routing(handle, ids=0, wts=0, offsets=0, perm=0, inv=0, stream=0) -> None:
