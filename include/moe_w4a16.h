@@ -76,6 +76,14 @@ enum moe_w4a16_status {
 #define MOE_W4A16_FLAG_FORCE_TC 0x2u     /* tensor-core experts at every size     */
                                          /* (create fails if hidden % 256 != 0)   */
 #define MOE_W4A16_FLAG_PROFILE 0x4u      /* time each kernel with CUDA events     */
+/* W4A8-FP8 experts ("Throughputmaxxing: DeepSeek-V4-Flash on Isambard-AI", "A
+ * pass through the model": e4m3 activations, one scale per token per 128
+ * elements, applied with the weight group scales to each 128-block's partial
+ * sum; include/moe_w4a8.h states the readings). The same weights and routing;
+ * the expert GEMMs quantise x and h to e4m3 and run on the fp8 tensor cores
+ * (mma.sync). Not with the FORCE flags; needs inter and shared_inter <= hidden;
+ * handles only (forward_noalloc refuses it). */
+#define MOE_W4A16_FLAG_W4A8 0x8u
 
 /* device error flag bits (moe_w4a16_check_device_errors) */
 #define MOE_W4A16_DEVERR_TIMEOUT 0x1u    /* a bounded wait gave up                */

@@ -160,3 +160,102 @@ def test_blocks_compose_to_the_oracle_expert():
     rel = np.linalg.norm(got - want) / np.linalg.norm(want)
     assert rel <= 5e-3
     assert np.abs(got - want).max() <= 2e-2 * np.abs(want).max() + 1e-3
+
+
+# ------------------------------------------------------------ the W4A8 layer
+from moe_synth.device import upload_layer, upload_tokens  # noqa: E402
+from tests import moe_cases as mc  # noqa: E402
+
+
+def _layer_w4a8(layer, tensors, max_tokens, bias=None):
+    s = layer.shape
+    t = dict(tensors)
+    if bias is not None:
+        t["router_bias"] = torch.from_numpy(np.asarray(bias, np.float32)).to(DEV)
+    return moe.MoeLayer(s.hidden, s.experts, s.top_k, s.inter, s.shared_inter, max_tokens, t,
+                        flags=moe.MOE_W4A16_FLAG_W4A8)
+
+
+def _w4a8_ref(layer, subset):
+    """The W4A8 oracle's output rows for ``subset``: each token's experts on
+    its own row (the fp8 blocks are per row, so this equals the batched
+    oracle), weights generated per expert from the shape's seeds."""
+    shape = layer.shape
+    r = mo.route(layer.x, layer.router_w, layer.router_b, shape.experts, shape.top_k)
+    x = mo.bf16_to_f64(layer.x)
+    shared = ms.expert_weights(shape, shape.experts) if shape.shared_inter else None
+    cache = {}
+    out = np.zeros((len(subset), shape.hidden))
+    for i, t in enumerate(subset):
+        row = x[t:t + 1]
+        acc = w8.swiglu_expert_w4a8(row, shared)[0] if shared is not None else np.zeros(shape.hidden)
+        for j in range(shape.top_k):
+            e = int(r["ids"][t, j])
+            if e not in cache:
+                cache[e] = ms.expert_weights(shape, e)
+            acc = acc + r["weights"][t, j] * w8.swiglu_expert_w4a8(row, cache[e])[0]
+        out[i] = acc
+    return r, out
+
+
+@pytest.fixture(scope="module")
+def tiny_w4a8():
+    shape = ms.CONFIGS["tiny16"]
+    return shape, upload_layer(mc.weights_of(shape), DEV)[0]
+
+
+@pytest.mark.parametrize("T", [1, 5, 16, 65, 200])
+def test_w4a8_layer_tiny(tiny_w4a8, T):
+    shape, tensors = tiny_w4a8
+    layer = mc.layer_with_tokens(shape, T)
+    want = w8.moe_forward_w4a8(layer.x, layer.router_w, layer.router_b, layer.experts,
+                               layer.shared, shape.top_k)
+    obj = _layer_w4a8(layer, tensors, T)
+    x = upload_tokens(layer.x, DEV)
+    out = obj.forward(x)
+    torch.cuda.synchronize()
+    assert moe.moe_w4a16_check_device_errors(obj.handle) == 0
+    rt = obj.routing(T)
+    names = [n for n, _ in moe.moe_w4a16_last_launches(obj.handle)]
+    obj.close()
+    mc.check_routing(rt, want, shape.experts)
+    mc.check_output(out.cpu().numpy(), want["out"])
+    assert "w4a8_gate_up_swiglu" in names and "w4a8_down" in names
+
+
+def test_w4a8_layer_differs_from_w4a16(tiny_w4a8):
+    """The flag changes the arithmetic: the W4A8 output is not the W4A16 one."""
+    shape, tensors = tiny_w4a8
+    layer = mc.layer_with_tokens(shape, 16)
+    x = upload_tokens(layer.x, DEV)
+    a = _layer_w4a8(layer, tensors, 16)
+    o8 = a.forward(x).cpu().numpy()
+    a.close()
+    t = dict(tensors)
+    b = moe.MoeLayer(shape.hidden, shape.experts, shape.top_k, shape.inter, shape.shared_inter, 16, t)
+    o16 = b.forward(x).cpu().numpy()
+    b.close()
+    assert (o8 != o16).mean() > 0.5
+
+
+@pytest.fixture(scope="module")
+def full_w4a8():
+    return upload_layer(mc.weights_of(ms.CONFIGS["decode1"]), DEV)[0]
+
+
+@pytest.mark.parametrize("name,n", [("decode1", 1), ("decode64", 6)])
+def test_w4a8_layer_full_size_sampled(full_w4a8, name, n):
+    shape = ms.CONFIGS[name]
+    tensors = full_w4a8
+    layer = mc.layer_with_tokens(shape)
+    T = shape.tokens
+    obj = _layer_w4a8(layer, tensors, T, bias=layer.router_b)
+    out = obj.forward(upload_tokens(layer.x, DEV))
+    torch.cuda.synchronize()
+    assert moe.moe_w4a16_check_device_errors(obj.handle) == 0
+    rt = obj.routing(T)
+    obj.close()
+    subset = np.linspace(0, T - 1, n).astype(np.int64)
+    r, want = _w4a8_ref(layer, subset)
+    mc.check_routing(rt, r, shape.experts)
+    mc.check_output(out.cpu().numpy()[subset], want)

@@ -25,6 +25,7 @@ MOE_W4A16_ERR_NO_DEVICE = -7
 MOE_W4A16_FLAG_FORCE_GEMV = 0x1
 MOE_W4A16_FLAG_FORCE_TC = 0x2
 MOE_W4A16_FLAG_PROFILE = 0x4
+MOE_W4A16_FLAG_W4A8 = 0x8
 
 # device error flag bits (moe_w4a16_check_device_errors)
 MOE_W4A16_DEVERR_TIMEOUT = 0x1

@@ -113,6 +113,25 @@ cudaError_t launch_tc_down(const Dims& d, const Routing& r, const TcWeights& w,
                            const CUtensorMap& hmap, uint16_t* y, int grid, cudaStream_t s,
                            LaunchLog& log);
 
+// W4A8-FP8 experts (csrc/w4a8.cu): x quantised to e4m3 per token per 128
+// (xc, xs), gate/up + SwiGLU into fp32 h (hf [rows, hst]), h quantised (hc,
+// hs), down into fp32 y [rows, H]; the tasks are the GEMV engine's (task1 /
+// task2 of the routing). The combine follows (launch_combine, fp32 y).
+struct W4a8Weights {
+  const uint32_t* w13_q;
+  const uint16_t* w13_s;
+  const uint32_t* w2_q;
+  const uint16_t* w2_s;
+  const uint32_t* sh_w13_q;
+  const uint16_t* sh_w13_s;
+  const uint32_t* sh_w2_q;
+  const uint16_t* sh_w2_s;
+};
+cudaError_t launch_w4a8_experts(const Dims& d, const Routing& r, const W4a8Weights& w,
+                                const uint16_t* x, uint8_t* xc, float* xs, float* hf, uint8_t* hc,
+                                float* hs, int hst, float* y, int grid, cudaStream_t s,
+                                LaunchLog& log);
+
 // y fp32 (the GEMV engine's) or bf16 (the tensor-core engine's)
 cudaError_t launch_combine(const Dims& d, const Routing& r, const float* y, uint16_t* out,
                            cudaStream_t s, LaunchLog& log);

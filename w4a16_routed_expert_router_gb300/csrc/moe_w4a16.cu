@@ -98,9 +98,13 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 int validate_config(const moe_w4a16_config* c) {
   if (!c) return MOE_W4A16_ERR_INVALID_ARG;
-  if (c->flags & ~(MOE_W4A16_FLAG_FORCE_GEMV | MOE_W4A16_FLAG_FORCE_TC | MOE_W4A16_FLAG_PROFILE))
+  if (c->flags & ~(MOE_W4A16_FLAG_FORCE_GEMV | MOE_W4A16_FLAG_FORCE_TC | MOE_W4A16_FLAG_PROFILE |
+                   MOE_W4A16_FLAG_W4A8))
     return MOE_W4A16_ERR_INVALID_ARG;
   if ((c->flags & MOE_W4A16_FLAG_FORCE_GEMV) && (c->flags & MOE_W4A16_FLAG_FORCE_TC))
+    return MOE_W4A16_ERR_INVALID_ARG;
+  if ((c->flags & MOE_W4A16_FLAG_W4A8) &&
+      (c->flags & (MOE_W4A16_FLAG_FORCE_GEMV | MOE_W4A16_FLAG_FORCE_TC)))
     return MOE_W4A16_ERR_INVALID_ARG;
   if (c->max_tokens < 1 || c->max_tokens > (1 << 20)) return MOE_W4A16_ERR_INVALID_ARG;
   if (c->group_size != kGroup) return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
@@ -109,6 +113,9 @@ int validate_config(const moe_w4a16_config* c) {
   if (c->shared_inter < 0 || c->shared_inter > 16384 || c->shared_inter % 128)
     return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
   if (c->num_experts < 1 || c->num_experts > kMaxExperts) return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
+  // W4A8 experts keep fp32 h in the y buffer: h is at most H wide
+  if ((c->flags & MOE_W4A16_FLAG_W4A8) && (c->inter > c->hidden || c->shared_inter > c->hidden))
+    return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
   if (c->top_k < 1 || c->top_k > kMaxTopK || c->top_k > c->num_experts)
     return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;
   // row counts of the stacked expert tensors must fit the int32 row indices
@@ -648,6 +655,32 @@ int moe_w4a16_forward(moe_w4a16_handle* h, const uint16_t* x, int32_t T, const m
 
   Dims d{T, c.hidden, c.num_experts, c.top_k, c.inter, c.shared_inter};
   cudaError_t e;
+  if (c.flags & MOE_W4A16_FLAG_W4A8) {
+    // W4A8-FP8 experts at every batch size: the GEMV engine's routing (no
+    // gather), e4m3 x codes and scales in the xperm buffer, fp32 h in y, e4m3
+    // h codes and scales in the h buffer, fp32 y, the combine
+    Routing rg = h->r;
+    rg.xperm = nullptr;
+    rg.task3 = rg.task4 = nullptr;
+    if ((e = launch_route(d, rg, x, w->router_w, w->router_bias, s, h->log)) != cudaSuccess)
+      return cuda_status(e);
+    const int hst = h->hstride;
+    const int rows = T * c.top_k + (c.shared_inter > 0 ? T : 0);
+    uint8_t* xc = reinterpret_cast<uint8_t*>(h->r.xperm);
+    float* xs = reinterpret_cast<float*>(xc + align256((size_t)T * c.hidden));
+    uint8_t* hc = reinterpret_cast<uint8_t*>(h->h);
+    float* hs = reinterpret_cast<float*>(hc + align256((size_t)rows * hst));
+    W4a8Weights ww{reinterpret_cast<const uint32_t*>(w->w13_q), w->w13_s,
+                   reinterpret_cast<const uint32_t*>(w->w2_q), w->w2_s,
+                   reinterpret_cast<const uint32_t*>(w->sh_w13_q), w->sh_w13_s,
+                   reinterpret_cast<const uint32_t*>(w->sh_w2_q), w->sh_w2_s};
+    if ((e = launch_w4a8_experts(d, h->r, ww, x, xc, xs, h->y, hc, hs, hst, h->y, h->gemv_grid, s,
+                                 h->log)) != cudaSuccess)
+      return cuda_status(e);
+    if ((e = launch_combine(d, h->r, h->y, out, s, h->log)) != cudaSuccess) return cuda_status(e);
+    h->last_T = T;
+    return MOE_W4A16_OK;
+  }
   if (T <= kSmallT && !(c.flags & MOE_W4A16_FLAG_FORCE_TC)) {
     // decode sizes: the whole layer in one cooperative persistent kernel
     if (!h->dec_ready || memcmp(&h->dec_key, w, sizeof(*w)) != 0) {
@@ -971,6 +1004,7 @@ extern "C" int moe_w4a16_forward_noalloc(const moe_w4a16_config* cfg, const uint
   int st = validate_config(cfg);
   if (st != MOE_W4A16_OK) return st;
   const moe_w4a16_config& c = *cfg;
+  if (c.flags & MOE_W4A16_FLAG_W4A8) return MOE_W4A16_ERR_UNSUPPORTED_SHAPE;  // handles only
   if (T < 0) return MOE_W4A16_ERR_INVALID_ARG;
   if (T > MOE_W4A16_NOALLOC_MAX_TOKENS) return MOE_W4A16_ERR_TOO_MANY_TOKENS;
   if ((st = validate_weights(c, w)) != MOE_W4A16_OK) return st;

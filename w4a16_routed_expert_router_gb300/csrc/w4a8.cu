@@ -20,6 +20,7 @@
 // channels x 8 rows); the weights' group scales and the rows' block scales
 // multiply each block's fp32 partial before it is added.
 #include "common.cuh"
+#include "kernels.h"
 #include "moe_w4a8.h"
 
 #include <cuda_fp8.h>
@@ -37,17 +38,25 @@ __device__ __forceinline__ uint16_t e4m3x2(float a, float b) {
   return r;
 }
 
-// x: [rows, K] fp32 (row stride K); codes [rows, K] e4m3 bytes; scales
-// [rows, K / 128] fp32. Warp w of the grid takes block (w / nb, w % nb); lane
-// l its elements 4l .. 4l + 3.
-__global__ void quantize_blocks_kernel(const float* __restrict__ x, int rows, int K,
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const uint16_t* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+
+// x: [rows, K] fp32 or bf16 (row stride K); codes [rows, K] e4m3 bytes;
+// scales [rows, K / 128] fp32. Warp w of the grid takes block (w / nb, w % nb);
+// lane l its elements 4l .. 4l + 3.
+template <typename In>
+__global__ void quantize_blocks_kernel(const In* __restrict__ x, int rows, int K,
                                        uint8_t* __restrict__ codes, float* __restrict__ scales) {
   const int nb = K / kBlk;
   const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= (long long)rows * nb) return;
   const int r = (int)(wid / nb), g = (int)(wid - (long long)r * nb);
-  const float4 v = *reinterpret_cast<const float4*>(x + (size_t)r * K + g * kBlk + 4 * lane);
+  const float4 v = load4(x + (size_t)r * K + g * kBlk + 4 * lane);
   const float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
   // non-negative floats order as their bit patterns
   const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
@@ -133,9 +142,197 @@ __global__ void linear_kernel(const uint8_t* __restrict__ codes, const float* __
   }
 }
 
+// ------------------------------------------------------------ the layer
+// One 16-channel x 8-row tile of the block-scaled product: A the INT4 weight
+// rows wr0 (channel gid) and wr1 (gid + 8) with their bf16 group scales ws0 /
+// ws1, B this lane's activation row (codes, or null: a padding row), D rows
+// scaled by sx0 / sx1 (null: padding). K a multiple of 128.
+__device__ __forceinline__ void tile_16x8(const uint32_t* wr0, const uint32_t* wr1,
+                                          const uint16_t* ws0, const uint16_t* ws1, int K,
+                                          const uint8_t* brow, const float* sx0,
+                                          const float* sx1, int tig, float (&acc)[4]) {
+  const int nb = K / kBlk;
+  for (int g = 0; g < nb; ++g) {
+    float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < kBlk / 32; ++ks) {
+      const int kb = g * kBlk + ks * 32;
+      const int wlo = (kb + 4 * tig) >> 3, shlo = ((4 * tig) & 7) * 4;
+      const int whi = (kb + 16 + 4 * tig) >> 3, shhi = ((16 + 4 * tig) & 7) * 4;
+      uint32_t a[4];
+      a[0] = int4x4_to_e4m3x4(__ldg(wr0 + wlo) >> shlo);
+      a[1] = int4x4_to_e4m3x4(__ldg(wr1 + wlo) >> shlo);
+      a[2] = int4x4_to_e4m3x4(__ldg(wr0 + whi) >> shhi);
+      a[3] = int4x4_to_e4m3x4(__ldg(wr1 + whi) >> shhi);
+      uint32_t b[2];
+      b[0] = brow ? *reinterpret_cast<const uint32_t*>(brow + kb + 4 * tig) : 0u;
+      b[1] = brow ? *reinterpret_cast<const uint32_t*>(brow + kb + 16 + 4 * tig) : 0u;
+      mma_e4m3_16832(part, a, b);
+    }
+    const float w0 = __uint_as_float((uint32_t)__ldg(ws0 + g) << 16);
+    const float w1 = __uint_as_float((uint32_t)__ldg(ws1 + g) << 16);
+    const float x0 = sx0 ? sx0[g] : 0.f, x1 = sx1 ? sx1[g] : 0.f;
+    acc[0] = fmaf(w0 * x0, part[0], acc[0]);
+    acc[1] = fmaf(w0 * x1, part[1], acc[1]);
+    acc[2] = fmaf(w1 * x0, part[2], acc[2]);
+    acc[3] = fmaf(w1 * x1, part[3], acc[3]);
+  }
+}
+
+struct W4a8Layer {
+  Dims d;
+  Routing r;
+  W4a8Weights w;
+  const uint8_t* xc;  // e4m3 x [T, H] (token order)
+  const float* xs;    // [T, H / 128]
+  float* hf;          // fp32 h [rows, hst] (expert-sorted rows)
+  const uint8_t* hc;  // e4m3 h [rows, hst]
+  const float* hs;    // [rows, hst / 128]
+  int hst;
+  float* y;           // fp32 [rows, H]
+};
+
+__device__ __forceinline__ int passes8(int rows) { return (rows + kPassRows - 1) / kPassRows; }
+
+// The expert tasks of the W4A16 GEMV engine (the routing lists their prefix
+// per active expert): the shared expert's first, then (expert, channel tile,
+// 8-row pass) in expert order. MODE 1: 16 gate + 16 up channels; MODE 2: 32
+// output channels. One warp per task, grid-stride.
+template <int MODE>
+__global__ void __launch_bounds__(256) grouped_kernel(const W4a8Layer L) {
+  const Dims& d = L.d;
+  const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+  const int ct_sh = MODE == 1 ? d.Is / kTile1 : d.H / kTile2;
+  const int n_sh = d.Is > 0 ? ct_sh * passes8(d.T) : 0;
+  const int n_act = L.r.meta[kMetaActive];
+  const int total = n_sh + L.r.meta[MODE == 1 ? kMetaTasks1 : kMetaTasks2];
+  const int* pre = MODE == 1 ? L.r.task1 : L.r.task2;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int tau = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; tau < total; tau += nwarps) {
+    bool sh;
+    int e, seg0, seg1, local;
+    if (tau < n_sh) {
+      sh = true;
+      e = d.E;
+      seg0 = d.T * d.k;
+      seg1 = seg0 + d.T;
+      local = tau;
+    } else {
+      sh = false;
+      const int tr = tau - n_sh;
+      int lo = 0, hi = n_act - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(pre + mid) <= tr) lo = mid;
+        else hi = mid - 1;
+      }
+      e = __ldg(L.r.active + lo);
+      seg0 = __ldg(L.r.offsets + e);
+      seg1 = __ldg(L.r.offsets + e + 1);
+      local = tr - __ldg(pre + lo);
+    }
+    const int passes = passes8(seg1 - seg0);
+    const int tile = local / passes, pass = local - tile * passes;
+    const int r0 = seg0 + pass * kPassRows, nr = min(kPassRows, seg1 - r0);
+    const int inter = sh ? d.Is : d.I;
+    // this lane's B row and the rows of its D values (expert-sorted row space)
+    const int rb = r0 + gid, rc0 = r0 + 2 * tig, rc1 = rc0 + 1;
+    const bool vb = gid < nr, v0 = 2 * tig < nr, v1 = 2 * tig + 1 < nr;
+    if (MODE == 1) {
+      // activations: x codes of the row's token
+      auto tok = [&](int row) { return sh ? row - d.T * d.k : __ldg(L.r.perm + row); };
+      const int nbx = d.H / kBlk;
+      const uint8_t* brow = vb ? L.xc + (size_t)tok(rb) * d.H : nullptr;
+      const float* s0 = v0 ? L.xs + (size_t)tok(rc0) * nbx : nullptr;
+      const float* s1 = v1 ? L.xs + (size_t)tok(rc1) * nbx : nullptr;
+      const uint32_t* wq = sh ? L.w.sh_w13_q : L.w.w13_q;
+      const uint16_t* wsc = sh ? L.w.sh_w13_s : L.w.w13_s;
+      const int rowg = (sh ? 0 : e * 2 * inter) + tile * kTile1, rowu = rowg + inter;
+      const int kw = d.H / 8;
+      float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+      tile_16x8(wq + (size_t)(rowg + gid) * kw, wq + (size_t)(rowg + gid + 8) * kw,
+                wsc + (size_t)(rowg + gid) * nbx, wsc + (size_t)(rowg + gid + 8) * nbx, d.H, brow,
+                s0, s1, tig, g);
+      tile_16x8(wq + (size_t)(rowu + gid) * kw, wq + (size_t)(rowu + gid + 8) * kw,
+                wsc + (size_t)(rowu + gid) * nbx, wsc + (size_t)(rowu + gid + 8) * nbx, d.H, brow,
+                s0, s1, tig, u);
+      const int c0 = tile * kTile1 + gid;
+      auto hv = [](float gg, float uu) { return gg / (1.0f + __expf(-gg)) * uu; };
+      if (v0) {
+        L.hf[(size_t)rc0 * L.hst + c0] = hv(g[0], u[0]);
+        L.hf[(size_t)rc0 * L.hst + c0 + 8] = hv(g[2], u[2]);
+      }
+      if (v1) {
+        L.hf[(size_t)rc1 * L.hst + c0] = hv(g[1], u[1]);
+        L.hf[(size_t)rc1 * L.hst + c0 + 8] = hv(g[3], u[3]);
+      }
+    } else {
+      // activations: this row's h codes (already in expert-sorted order)
+      const int nbh = L.hst / kBlk, nbk = inter / kBlk;
+      const uint8_t* brow = vb ? L.hc + (size_t)rb * L.hst : nullptr;
+      const float* s0 = v0 ? L.hs + (size_t)rc0 * nbh : nullptr;
+      const float* s1 = v1 ? L.hs + (size_t)rc1 * nbh : nullptr;
+      const uint32_t* wq = sh ? L.w.sh_w2_q : L.w.w2_q;
+      const uint16_t* wsc = sh ? L.w.sh_w2_s : L.w.w2_s;
+      const int kw = inter / 8;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int row = (sh ? 0 : e * d.H) + tile * kTile2 + 16 * half;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_16x8(wq + (size_t)(row + gid) * kw, wq + (size_t)(row + gid + 8) * kw,
+                  wsc + (size_t)(row + gid) * nbk, wsc + (size_t)(row + gid + 8) * nbk, inter, brow,
+                  s0, s1, tig, acc);
+        const int c0 = tile * kTile2 + 16 * half + gid;
+        if (v0) {
+          L.y[(size_t)rc0 * d.H + c0] = acc[0];
+          L.y[(size_t)rc0 * d.H + c0 + 8] = acc[2];
+        }
+        if (v1) {
+          L.y[(size_t)rc1 * d.H + c0] = acc[1];
+          L.y[(size_t)rc1 * d.H + c0 + 8] = acc[3];
+        }
+      }
+    }
+  }
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+cudaError_t launch_w4a8_experts(const Dims& d, const Routing& r, const W4a8Weights& w,
+                                const uint16_t* x, uint8_t* xc, float* xs, float* hf, uint8_t* hc,
+                                float* hs, int hst, float* y, int grid, cudaStream_t s,
+                                LaunchLog& log) {
+  cudaError_t e;
+  const int rows = d.T * d.k + (d.Is > 0 ? d.T : 0);
+  log.begin("w4a8_quantize_x", s);
+  {
+    const long long warps = (long long)d.T * (d.H / kBlk);
+    quantize_blocks_kernel<uint16_t><<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(
+        x, d.T, d.H, xc, xs);
+  }
+  log.end(s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  W4a8Layer L{d, r, w, xc, xs, hf, hc, hs, hst, y};
+  log.begin("w4a8_gate_up_swiglu", s);
+  grouped_kernel<1><<<grid, 256, 0, s>>>(L);
+  log.end(s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  log.begin("w4a8_quantize_h", s);
+  {
+    const long long warps = (long long)rows * (hst / kBlk);
+    quantize_blocks_kernel<float><<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(
+        hf, rows, hst, hc, hs);
+  }
+  log.end(s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  log.begin("w4a8_down", s);
+  grouped_kernel<2><<<grid, 256, 0, s>>>(L);
+  log.end(s);
+  return cudaGetLastError();
+}
+
 }  // namespace moe
 
 extern "C" int moe_w4a8_quantize_blocks(const float* x, int32_t rows, int32_t K, uint8_t* codes,
@@ -148,7 +345,7 @@ extern "C" int moe_w4a8_quantize_blocks(const float* x, int32_t rows, int32_t K,
   const int threads = 256;
   const long long blocks = (warps * 32 + threads - 1) / threads;
   if (blocks > 0x7fffffffLL) return MOE_W4A8_INVALID_ARG;
-  moe::quantize_blocks_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
+  moe::quantize_blocks_kernel<float><<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
       x, rows, K, codes, scales);
   return cudaGetLastError() == cudaSuccess ? MOE_W4A8_OK : MOE_W4A8_CUDA_ERROR;
 }
