@@ -101,6 +101,15 @@ def kernel_work(name, shape, work, y_bytes=None):
         return work["w2_bytes"] + hrows * 2 + rows * H * 4, f2
     if name.startswith("tc_down"):
         return work["w2_bytes"] + hrows * 2 + rows * H * 2, f2
+    # W4A8-FP8 experts: e4m3 activations (1 byte) in, fp32 h and y out
+    if name == "w4a8_quantize_x":
+        return T * H * 2 + T * H + T * (H // 128) * 4, 0
+    if name == "w4a8_gate_up_swiglu":
+        return work["w13_bytes"] + T * H + T * (H // 128) * 4 + hrows * 4, f13
+    if name == "w4a8_quantize_h":
+        return hrows * 4 + hrows + hrows // 128 * 4, 0
+    if name == "w4a8_down":
+        return work["w2_bytes"] + hrows + hrows // 128 * 4 + rows * H * 4, f2
     if name.startswith("route") or name.startswith("router"):
         return work["router_bytes"] + T * H * 2 * 2, 2 * T * E * H
     if name == "combine":
@@ -123,14 +132,18 @@ def roofline(name, shape, work, seconds, pk, y_bytes=None):
     bounds is slower for its algorithmic work decides the bound."""
     nbytes, flops = kernel_work(name, shape, work, y_bytes)
     extra = implementation_bytes(name, shape)
+    # fp8 kernels: the measured bf16 peak times the nominal fp8 / bf16 ratio (2)
+    fp8 = name.startswith("w4a8")
+    tpk = pk["bf16_tflops"] * (2.0 if fp8 else 1.0)
     t_mem = nbytes / (pk["hbm_gbs"] * 1e9)
-    t_mma = flops / (pk["bf16_tflops"] * 1e12)
+    t_mma = flops / (tpk * 1e12)
     if t_mma > t_mem:
         ach = flops / seconds / 1e12
-        return {"kernel": name, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "algorithmic_flops": flops,
+        return {"kernel": name, "bound": "tensor", "achieved": ach, "peak": tpk,
+                "unit": "TFLOP/s", "frac": ach / tpk, "algorithmic_flops": flops,
                 "algorithmic_bytes": nbytes, "implementation_bytes": extra,
-                "peak_source": pk["source"] + " (burst)"}
+                "peak_source": pk["source"] + (" bf16 x 2 (fp8, nominal ratio)" if fp8 else "")
+                               + " (burst)"}
     ach = nbytes / seconds / 1e9
     return {"kernel": name, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
             "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "algorithmic_bytes": nbytes,
@@ -234,13 +247,16 @@ def max_over_ranks(value, dist, device=None):
 
 
 # ------------------------------------------------------------ CPU oracle arm
-def oracle_sample(shape, budget_s=15.0):
+def oracle_sample(shape, budget_s=15.0, w4a8=False):
     """Time the fp64 oracle on the host on a bounded sample of the workload.
 
     Routing is computed for the whole batch; outputs token by token until the
-    time budget is spent. Drawing the synthetic weights is not timed.
+    time budget is spent. Drawing the synthetic weights is not timed. w4a8:
+    the W4A8-FP8 oracle's layer instead of the W4A16 one.
     """
     from oracle import moe_oracle as mo
+    from oracle import w4a8_oracle as w8
+    layer_fn = w8.moe_forward_w4a8 if w4a8 else mo.moe_forward
     x = ms.tokens(shape)
     rw, rb = ms.router_weights(shape), ms.router_bias(shape)
     shared = ms.expert_weights(shape, shape.experts) if shape.shared_inter else None
@@ -262,7 +278,7 @@ def oracle_sample(shape, budget_s=15.0):
         for e in route["ids"][t]:
             experts[int(e)] = ms.expert_weights(shape, int(e))
         t0, c0 = time.perf_counter(), time.process_time()
-        mo.moe_forward(x[t:t + 1], rw, rb, experts, shared, shape.top_k)
+        layer_fn(x[t:t + 1], rw, rb, experts, shared, shape.top_k)
         wall += time.perf_counter() - t0
         cpu += time.process_time() - c0
         done += 1
@@ -348,7 +364,8 @@ class Bench:
                             dev) for i in range(nx)]
         out = torch.empty((T, H), dtype=torch.int16, device=dev)
         path_flags = {"auto": 0, "tc": moe.MOE_W4A16_FLAG_FORCE_TC,
-                      "gemv": moe.MOE_W4A16_FLAG_FORCE_GEMV}[self.args.expert_path]
+                      "gemv": moe.MOE_W4A16_FLAG_FORCE_GEMV,
+                      "w4a8": moe.MOE_W4A16_FLAG_W4A8}[self.args.expert_path]
         obj = moe.MoeLayer(shape.hidden, shape.experts, shape.top_k, shape.inter,
                            shape.shared_inter, T, tensors, flags=path_flags)
         prof = moe.MoeLayer(shape.hidden, shape.experts, shape.top_k, shape.inter,
@@ -443,7 +460,7 @@ class Bench:
         prof.close()
 
         pk = peaks()
-        y_bytes = 4 if any(n.startswith("gemv_down") for n in kernel_avg) else 2
+        y_bytes = 4 if any(n.startswith(("gemv_down", "w4a8_down")) for n in kernel_avg) else 2
         roof = roofline(dominant, shape, work, kernel_avg[dominant] / 1000.0, pk, y_bytes)
         roof["traffic"] = profiled_traffic(dominant, shape.name)
         layer_roof_s = max(work["bytes"] / (pk["hbm_gbs"] * 1e9),
@@ -494,12 +511,13 @@ def run_ours(args, shape):
         others[name] = r
 
     if rank == 0:
-        cpu = oracle_sample(shape, budget_s=15.0) if world == 1 else None
+        cpu = oracle_sample(shape, budget_s=15.0, w4a8=args.expert_path == "w4a8") if world == 1 else None
         line = {
             "metric": METRIC, "value": head["value"], "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": head["ms_per_step"],
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3" if args.expert_path == "w4a8" else "bf16",
             "data": "synthetic",
             "config": config_of(shape, args),
         }
@@ -527,8 +545,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="decode1", choices=ms.CONFIG_ORDER)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--expert-path", default="auto", choices=["auto", "tc", "gemv"],
-                    help="expert kernels: the library's choice, tensor-core, or split-K GEMV")
+    ap.add_argument("--expert-path", default="auto", choices=["auto", "tc", "gemv", "w4a8"],
+                    help="expert kernels: the library's choice, tensor-core, split-K GEMV, "
+                         "or the W4A8-FP8 experts (e4m3 activations)")
     ap.add_argument("--per-config", default="decode64,prefill8192,zipf2048",
                     help="further workloads measured after the headline one and reported "
                          "under per_config (comma-separated; 'none' for none)")
