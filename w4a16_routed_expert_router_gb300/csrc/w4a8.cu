@@ -315,6 +315,9 @@ cudaError_t launch_w4a8_experts(const Dims& d, const Routing& r, const W4a8Weigh
   log.end(s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   W4a8Layer L{d, r, w, xc, xs, hf, hc, hs, hst, y};
+  // four 8-warp blocks per SM (64 registers a thread): the tasks' plain weight
+  // loads need the warps in flight
+  grid *= 4;
   log.begin("w4a8_gate_up_swiglu", s);
   grouped_kernel<1><<<grid, 256, 0, s>>>(L);
   log.end(s);
