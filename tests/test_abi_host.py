@@ -111,6 +111,12 @@ def test_workspace_bytes_of_a_valid_config(L):
     (dict(flags=0x100), moe.MOE_W4A16_ERR_INVALID_ARG),
     (dict(flags=moe.MOE_W4A16_FLAG_FORCE_GEMV | moe.MOE_W4A16_FLAG_FORCE_TC),
      moe.MOE_W4A16_ERR_INVALID_ARG),
+    # W4A8 experts: not with a FORCE flag; fp32 h lives in y, so h <= hidden
+    (dict(flags=moe.MOE_W4A16_FLAG_W4A8 | moe.MOE_W4A16_FLAG_FORCE_TC), moe.MOE_W4A16_ERR_INVALID_ARG),
+    (dict(flags=moe.MOE_W4A16_FLAG_W4A8 | moe.MOE_W4A16_FLAG_FORCE_GEMV), moe.MOE_W4A16_ERR_INVALID_ARG),
+    (dict(flags=moe.MOE_W4A16_FLAG_W4A8, hidden=1024, inter=2048), moe.MOE_W4A16_ERR_UNSUPPORTED_SHAPE),
+    (dict(flags=moe.MOE_W4A16_FLAG_W4A8, hidden=1024, inter=512, shared_inter=2048),
+     moe.MOE_W4A16_ERR_UNSUPPORTED_SHAPE),
 ])
 def test_invalid_configs_are_rejected(L, kw, status):
     with pytest.raises(moe.MoeError) as ei:
@@ -119,6 +125,17 @@ def test_invalid_configs_are_rejected(L, kw, status):
     h = ctypes.c_void_p()
     assert L.moe_w4a16_create(ctypes.byref(_cfg(**kw)), 0, ctypes.byref(h)) == status
     assert not h.value
+
+
+def test_w4a8_flag_is_a_valid_config(L):
+    assert moe.moe_w4a16_workspace_bytes(_cfg(flags=moe.MOE_W4A16_FLAG_W4A8)) == \
+        moe.moe_w4a16_workspace_bytes(_cfg())          # no extra workspace
+
+
+def test_noalloc_refuses_the_w4a8_flag_before_any_device_work(L):
+    c = _cfg(flags=moe.MOE_W4A16_FLAG_W4A8, max_tokens=16)
+    assert L.moe_w4a16_forward_noalloc(ctypes.byref(c), None, 1, None, None, None) == \
+        moe.MOE_W4A16_ERR_UNSUPPORTED_SHAPE
 
 
 def test_group_size_must_be_128(L):

@@ -95,3 +95,25 @@ def test_both_arms_print_the_same_config():
     shape = ms.CONFIGS["decode1"]
     c = bench.config_of(shape, args)
     assert c["workload"] == "decode1" and c["tokens"] == 1 and c["experts"] == 256
+
+
+def test_w4a8_kernel_work():
+    """The W4A8 path's kernels: the same weight bytes, e4m3 activations (one
+    byte, one fp32 scale per 128), fp32 h and y; the fp8 tensor peak is the
+    measured bf16 one times the nominal ratio 2."""
+    shape = ms.CONFIGS["decode64"]
+    work = bench.layer_work(shape, _counts(shape, 150))
+    T, H, k, I, Is = 64, 4096, 6, 2048, 2048
+    hrows = T * k * I + T * Is
+    rows = T * k + T
+    b13, f13 = bench.kernel_work("w4a8_gate_up_swiglu", shape, work)
+    assert b13 == work["w13_bytes"] + T * H + T * (H // 128) * 4 + hrows * 4
+    assert f13 == 2 * H * 2 * hrows
+    b2, f2 = bench.kernel_work("w4a8_down", shape, work)
+    assert b2 == work["w2_bytes"] + hrows + hrows // 128 * 4 + rows * H * 4
+    assert f2 == 2 * H * hrows
+    assert bench.kernel_work("w4a8_quantize_x", shape, work) == (T * H * 3 + T * 32 * 4, 0)
+    p = ms.CONFIGS["prefill8192"]
+    wp = bench.layer_work(p, np.full(p.experts, 192))
+    r = bench.roofline("w4a8_gate_up_swiglu", p, wp, 1.0e-3, MEASURED)
+    assert r["bound"] == "tensor" and r["peak"] == 2 * 1885.7
