@@ -23,7 +23,6 @@
 #include "kernels.h"
 #include "moe_w4a8.h"
 
-
 namespace moe {
 namespace {
 
