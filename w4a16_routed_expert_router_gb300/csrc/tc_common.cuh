@@ -37,7 +37,7 @@ __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, unsigned* 
   }
 }
 
-// the same wait by every lane of a warp, with one verdict for the warp (the
+// the same wait by every lane of a warp, with one outcome for the warp (the
 // tcgen05.ld that follows is warp-collective)
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
   const bool ok = bwait(bar, parity, err);
