@@ -141,16 +141,16 @@ __global__ void linear_kernel(const uint8_t* __restrict__ codes, const float* __
 }
 
 // ------------------------------------------------------------ the layer
-// One 16-channel x 8-row tile of the block-scaled product: A the INT4 weight
-// rows wr0 (channel gid) and wr1 (gid + 8) with their bf16 group scales ws0 /
-// ws1, B this lane's activation row (codes, or null: a padding row), D rows
-// scaled by sx0 / sx1 (null: padding). K a multiple of 128.
+// One 16-channel x 8-row tile of the block-scaled product over the 128-blocks
+// g = g0, g0 + gstep, ... < nb: A the INT4 weight rows wr0 (channel gid) and
+// wr1 (gid + 8) with their bf16 group scales ws0 / ws1, B this lane's
+// activation row (codes, or null: a padding row), D rows scaled by sx0 / sx1
+// (null: padding).
 __device__ __forceinline__ void tile_16x8(const uint32_t* wr0, const uint32_t* wr1,
-                                          const uint16_t* ws0, const uint16_t* ws1, int K,
-                                          const uint8_t* brow, const float* sx0,
+                                          const uint16_t* ws0, const uint16_t* ws1, int nb, int g0,
+                                          int gstep, const uint8_t* brow, const float* sx0,
                                           const float* sx1, int tig, float (&acc)[4]) {
-  const int nb = K / kBlk;
-  for (int g = 0; g < nb; ++g) {
+  for (int g = g0; g < nb; g += gstep) {
     float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ks = 0; ks < kBlk / 32; ++ks) {
@@ -195,18 +195,22 @@ __device__ __forceinline__ int passes8(int rows) { return (rows + kPassRows - 1)
 // The expert tasks of the W4A16 GEMV engine (the routing lists their prefix
 // per active expert): the shared expert's first, then (expert, channel tile,
 // 8-row pass) in expert order. MODE 1: 16 gate + 16 up channels; MODE 2: 32
-// output channels. One warp per task, grid-stride.
+// output channels. One block of kSplit warps per task (grid-stride): warp w
+// takes the 128-blocks w, w + kSplit, ... of K; warp 0 adds the warps'
+// partials in warp order and writes the result.
+constexpr int kSplit = 4;
 template <int MODE>
-__global__ void __launch_bounds__(256) grouped_kernel(const W4a8Layer L) {
+__global__ void __launch_bounds__(kSplit * 32) grouped_kernel(const W4a8Layer L) {
+  __shared__ float red[kSplit][32][8];
   const Dims& d = L.d;
+  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
   const int ct_sh = MODE == 1 ? d.Is / kTile1 : d.H / kTile2;
   const int n_sh = d.Is > 0 ? ct_sh * passes8(d.T) : 0;
   const int n_act = L.r.meta[kMetaActive];
   const int total = n_sh + L.r.meta[MODE == 1 ? kMetaTasks1 : kMetaTasks2];
   const int* pre = MODE == 1 ? L.r.task1 : L.r.task2;
-  const int nwarps = (gridDim.x * blockDim.x) >> 5;
-  for (int tau = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; tau < total; tau += nwarps) {
+  for (int tau = blockIdx.x; tau < total; tau += gridDim.x) {
     bool sh;
     int e, seg0, seg1, local;
     if (tau < n_sh) {
@@ -249,21 +253,41 @@ __global__ void __launch_bounds__(256) grouped_kernel(const W4a8Layer L) {
       const int kw = d.H / 8;
       float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
       tile_16x8(wq + (size_t)(rowg + gid) * kw, wq + (size_t)(rowg + gid + 8) * kw,
-                wsc + (size_t)(rowg + gid) * nbx, wsc + (size_t)(rowg + gid + 8) * nbx, d.H, brow,
-                s0, s1, tig, g);
+                wsc + (size_t)(rowg + gid) * nbx, wsc + (size_t)(rowg + gid + 8) * nbx, nbx, warp,
+                kSplit, brow, s0, s1, tig, g);
       tile_16x8(wq + (size_t)(rowu + gid) * kw, wq + (size_t)(rowu + gid + 8) * kw,
-                wsc + (size_t)(rowu + gid) * nbx, wsc + (size_t)(rowu + gid + 8) * nbx, d.H, brow,
-                s0, s1, tig, u);
+                wsc + (size_t)(rowu + gid) * nbx, wsc + (size_t)(rowu + gid + 8) * nbx, nbx, warp,
+                kSplit, brow, s0, s1, tig, u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        red[warp][lane][i] = g[i];
+        red[warp][lane][4 + i] = u[i];
+      }
+      __syncthreads();
+      if (warp == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          g[i] = red[0][lane][i];
+          u[i] = red[0][lane][4 + i];
+        }
+        for (int w = 1; w < kSplit; ++w)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            g[i] += red[w][lane][i];
+            u[i] += red[w][lane][4 + i];
+          }
+      }
       const int c0 = tile * kTile1 + gid;
       auto hv = [](float gg, float uu) { return gg / (1.0f + __expf(-gg)) * uu; };
-      if (v0) {
+      if (warp == 0 && v0) {
         L.hf[(size_t)rc0 * L.hst + c0] = hv(g[0], u[0]);
         L.hf[(size_t)rc0 * L.hst + c0 + 8] = hv(g[2], u[2]);
       }
-      if (v1) {
+      if (warp == 0 && v1) {
         L.hf[(size_t)rc1 * L.hst + c0] = hv(g[1], u[1]);
         L.hf[(size_t)rc1 * L.hst + c0 + 8] = hv(g[3], u[3]);
       }
+      __syncthreads();  // red is rewritten by the next task
     } else {
       // activations: this row's h codes (already in expert-sorted order)
       const int nbh = L.hst / kBlk, nbk = inter / kBlk;
@@ -273,23 +297,46 @@ __global__ void __launch_bounds__(256) grouped_kernel(const W4a8Layer L) {
       const uint32_t* wq = sh ? L.w.sh_w2_q : L.w.w2_q;
       const uint16_t* wsc = sh ? L.w.sh_w2_s : L.w.w2_s;
       const int kw = inter / 8;
+      float acc[2][4] = {};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int row = (sh ? 0 : e * d.H) + tile * kTile2 + 16 * half;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
         tile_16x8(wq + (size_t)(row + gid) * kw, wq + (size_t)(row + gid + 8) * kw,
-                  wsc + (size_t)(row + gid) * nbk, wsc + (size_t)(row + gid + 8) * nbk, inter, brow,
-                  s0, s1, tig, acc);
-        const int c0 = tile * kTile2 + 16 * half + gid;
-        if (v0) {
-          L.y[(size_t)rc0 * d.H + c0] = acc[0];
-          L.y[(size_t)rc0 * d.H + c0 + 8] = acc[2];
+                  wsc + (size_t)(row + gid) * nbk, wsc + (size_t)(row + gid + 8) * nbk, nbk, warp,
+                  kSplit, brow, s0, s1, tig, acc[half]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        red[warp][lane][i] = acc[0][i];
+        red[warp][lane][4 + i] = acc[1][i];
+      }
+      __syncthreads();
+      if (warp == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[0][i] = red[0][lane][i];
+          acc[1][i] = red[0][lane][4 + i];
         }
-        if (v1) {
-          L.y[(size_t)rc1 * d.H + c0] = acc[1];
-          L.y[(size_t)rc1 * d.H + c0 + 8] = acc[3];
+        for (int w = 1; w < kSplit; ++w)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[0][i] += red[w][lane][i];
+            acc[1][i] += red[w][lane][4 + i];
+          }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int c0 = tile * kTile2 + 16 * half + gid;
+          if (v0) {
+            L.y[(size_t)rc0 * d.H + c0] = acc[half][0];
+            L.y[(size_t)rc0 * d.H + c0 + 8] = acc[half][2];
+          }
+          if (v1) {
+            L.y[(size_t)rc1 * d.H + c0] = acc[half][1];
+            L.y[(size_t)rc1 * d.H + c0 + 8] = acc[half][3];
+          }
         }
       }
+      __syncthreads();  // red is rewritten by the next task
     }
   }
 }
@@ -313,11 +360,10 @@ cudaError_t launch_w4a8_experts(const Dims& d, const Routing& r, const W4a8Weigh
   log.end(s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   W4a8Layer L{d, r, w, xc, xs, hf, hc, hs, hst, y};
-  // four 8-warp blocks per SM (64 registers a thread): the tasks' plain weight
-  // loads need the warps in flight
+  // four 4-warp blocks per SM, all resident (up to 108 registers a thread)
   grid *= 4;
   log.begin("w4a8_gate_up_swiglu", s);
-  grouped_kernel<1><<<grid, 256, 0, s>>>(L);
+  grouped_kernel<1><<<grid, kSplit * 32, 0, s>>>(L);
   log.end(s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   log.begin("w4a8_quantize_h", s);
@@ -329,7 +375,7 @@ cudaError_t launch_w4a8_experts(const Dims& d, const Routing& r, const W4a8Weigh
   log.end(s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   log.begin("w4a8_down", s);
-  grouped_kernel<2><<<grid, 256, 0, s>>>(L);
+  grouped_kernel<2><<<grid, kSplit * 32, 0, s>>>(L);
   log.end(s);
   return cudaGetLastError();
 }
